@@ -1,0 +1,449 @@
+"""Benchmark of the KV wire codec hot path on the Qwen3-8B-shaped workload.
+
+One step = one pass of the whole path over one batch: encode every cached
+block of all 36 layers from the fp16 paged buffer to the FP8 E4M3 wire
+(gather + amax + scale + quantize + wire write), build the delta-m rotation
+table, and fetch every block back (dequantize + rotate K by delta-m +
+scatter into a bf16 paged buffer through a shuffled block table).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is algorithmic bytes moved per second over
+the whole job (all ranks), with inputs resident in HBM; `e2e` is the same
+metric with the source copied from pinned host memory and the result copied
+back inside the timed region; `cpu_baseline` / `--impl reference` time the
+float64 oracle on the host cores on a bounded sample of the same workload.
+Under torchrun each rank runs an independent replica (weak scaling: the path
+has no exchange step).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV fetch+rotate+scatter GB/s and tokens/s; % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = {
+    "k_encode_fp8": ["encode.cu", "hc_internal.cuh"],
+    "k_fetch": ["fetch_impl.cuh", "fetch_fp8.cu", "hc_internal.cuh"],
+}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_max_sum(seconds, units, backend_group=None):
+    """(max seconds over ranks, sum of units over ranks); identity at N = 1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return seconds, units
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(kernel):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "kv_cache_quantization_hc_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch recorded by ncu in profiles/, if the kernel's
+    sources are unchanged since; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
+            k, v = line.split(":", 1)
+            vals[k.strip().strip("-* `")] = v.strip().strip("`")
+    if vals.get("source_sha256") != kernel_source_hash(kernel):
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7], float(parts[7])))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r[3] > 0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in loaded for n, v in zip(names, r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+# ------------------------------------------------------------------ workload
+def algorithmic_bytes(w, blk):
+    """Bytes the method must move, per kernel, for one call over all layers."""
+    L, H, d, T, NB = w.L, w.H, w.d, blk.tokens(), blk.nb
+    src_b = {"f32": 4, "f16": 2, "bf16": 2}[w.src_dtype]
+    out_b = {"f32": 4, "f16": 2, "bf16": 2}[w.out_dtype]
+    kv_elems = 2 * L * T * H * d
+    codes = kv_elems
+    scales = L * NB * 2 * H * 4
+    n_distinct = len(np.unique(blk.delta_m))
+    table = n_distinct * (d // 2) * 8
+    encode = kv_elems * src_b + codes + scales + NB * 4
+    fetch = codes + scales + kv_elems * out_b + table + NB * 3 * 4
+    return {"encode": encode, "table": table + n_distinct * 4, "fetch": fetch}
+
+
+def setup_device(w, blk, device):
+    import torch
+    from kv_cache_quantization_hc_gb300 import path as kvpath
+    import workloads
+    src_k = workloads.device_pool(w, blk, range(w.L), 0, device)
+    src_v = workloads.device_pool(w, blk, range(w.L), 1, device)
+    shape = (w.L, blk.num_dst_slots, blk.B, w.H, w.d)
+    dst_k = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    dst_v = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    p = kvpath.from_blocks(w, blk, "fp8", device=device)
+    return p, src_k, src_v, dst_k, dst_v
+
+
+def run_ours(args):
+    import torch
+    import __graft_entry__
+    import workloads
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+
+    w = workloads.qwen3_8b()
+    if args.layers:
+        w.L = args.layers
+    blk = w.blocks[0]
+    p, src_k, src_v, dst_k, dst_v = setup_device(w, blk, device)
+    nbytes = algorithmic_bytes(w, blk)
+    step_bytes = sum(nbytes.values())
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        p.encode(src_k, src_v, stream=stream)
+        if ev: ev[1].record(stream)
+        p.build_table(stream=stream)
+        if ev: ev[2].record(stream)
+        p.fetch(dst_k, dst_v, stream=stream)
+        if ev: ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if p.error_bits():
+        raise RuntimeError(f"device error flag {p.error_bits()}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize(device)
+        start.record(stream)
+        for i in range(args.steps):
+            step(events[i])
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+    total_s = start.elapsed_time(end) / 1e3
+    per = {"encode": [], "table": [], "fetch": []}
+    for ev in events:
+        per["encode"].append(ev[0].elapsed_time(ev[1]) / 1e3)
+        per["table"].append(ev[1].elapsed_time(ev[2]) / 1e3)
+        per["fetch"].append(ev[2].elapsed_time(ev[3]) / 1e3)
+    if p.error_bits():
+        raise RuntimeError(f"device error flag {p.error_bits()}")
+
+    max_s, total_bytes = reduce_max_sum(total_s, step_bytes * args.steps)
+    _, total_tokens = reduce_max_sum(total_s, blk.tokens() * args.steps)
+    peak, peak_kind = measured_peaks()
+    kern = {}
+    for k in ("encode", "table", "fetch"):
+        avg = statistics.mean(per[k])
+        kern[k] = {"avg_ms": avg * 1e3, "min_ms": min(per[k]) * 1e3,
+                   "bytes_per_launch": nbytes[k], "gbs": nbytes[k] / avg / 1e9}
+    dominant = max(("encode", "fetch"), key=lambda k: kern[k]["avg_ms"])
+    kname = {"encode": "k_encode_fp8", "fetch": "k_fetch"}[dominant]
+    traffic = profiled_traffic(kname, "qwen3_8b") if not args.layers else None
+    achieved = kern[dominant]["gbs"]
+
+    e2e = None
+    if "e2e" in args.legs:
+        e2e = run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device)
+    cpu = None
+    if "cpu" in args.legs and rank == 0 and world == 1:
+        cpu = cpu_baseline(w, blk, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": total_bytes / max_s / 1e9, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": max_s / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"qwen3_8b: {w.L} layers x {w.H} KV heads x d{w.d}, "
+                                   f"{blk.tokens()} tokens, block {blk.B}, fp16 paged -> FP8 E4M3 "
+                                   f"wire (per-block-head fp32 scale) -> bf16 paged, delta-m +4096, "
+                                   f"half-split RoPE base 1e6, shuffled block tables",
+                       "layers": w.L, "tokens": blk.tokens(), "block_size": blk.B,
+                       "storage": {"source": w.src_dtype, "wire": "e4m3", "destination": w.out_dtype},
+                       "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (working set %.1f GB per step)" % (step_bytes / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "tokens_per_s": total_tokens / max_s,
+            "hbm_frac": total_bytes / max_s / 1e9 / world / peak,
+            "kernels": kern,
+            "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "algorithmic_bytes_per_launch": nbytes[dominant]},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device):
+    """Same step through the C ABI with host buffers: pinned host -> device copy
+    of the source K/V and the block tables, the three calls, device -> pinned
+    host copy of the fetched K/V, all inside the timed region."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    h_src_k = torch.empty(src_k.shape, dtype=src_k.dtype, pin_memory=True)
+    h_src_v = torch.empty(src_v.shape, dtype=src_v.dtype, pin_memory=True)
+    h_src_k.copy_(src_k)
+    h_src_v.copy_(src_v)
+    h_dst_k = torch.empty(dst_k.shape, dtype=dst_k.dtype, pin_memory=True)
+    h_dst_v = torch.empty(dst_v.shape, dtype=dst_v.dtype, pin_memory=True)
+    tables = [p.src_slots, p.dst_slots, p.delta_m, p.delta_idx]
+    h_tables = [t.cpu().pin_memory() for t in tables]
+    h2d = sum(t.numel() * t.element_size() for t in (h_src_k, h_src_v, *h_tables))
+    d2h = sum(t.numel() * t.element_size() for t in (h_dst_k, h_dst_v)) + 4
+    h_err = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def step():
+        src_k.copy_(h_src_k, non_blocking=True)
+        src_v.copy_(h_src_v, non_blocking=True)
+        for d_t, h_t in zip(tables, h_tables):
+            d_t.copy_(h_t, non_blocking=True)
+        p.encode(src_k, src_v, stream=stream)
+        p.build_table(stream=stream)
+        p.fetch(dst_k, dst_v, stream=stream)
+        h_dst_k.copy_(dst_k, non_blocking=True)
+        h_dst_v.copy_(dst_v, non_blocking=True)
+        h_err.copy_(p.err, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(device)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    if int(h_err.item()):
+        raise RuntimeError("device error flag set in e2e leg")
+    secs, total = reduce_max_sum(a.elapsed_time(b) / 1e3, step_bytes * steps)
+    return {"value": total / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_sample(w, blk, n_blocks, seed=0):
+    """A bounded sample of the workload for the oracle: one layer, the first
+    n_blocks blocks, source drawn on the host with the workload's distribution."""
+    r = np.random.default_rng(seed)
+    B, H, d = blk.B, w.H, w.d
+    from oracle.numerics import round_to
+    shape = (1, n_blocks, B, H, d)
+    k = round_to(r.standard_normal(shape) * 0.5, w.src_dtype)
+    v = round_to(r.standard_normal(shape) * 0.5, w.src_dtype)
+    return k, v
+
+
+def time_oracle_step(w, blk, k, v):
+    """One oracle pass over the sample: encode FP8, decode, rotate+scatter."""
+    from oracle import paged, rope
+    nb = k.shape[1]
+    th = rope.inv_freq(w.d, w.rope_base)
+    t0 = time.perf_counter()
+    codes, scales = paged.encode_fp8(k, v, np.arange(nb))
+    vals = paged.decode_fp8(codes, scales)
+    dm_vals = np.unique(blk.delta_m[:nb])
+    paged.delta_sincos_table(dm_vals, th)
+    out = np.zeros((1, nb, blk.B, w.H, w.d))
+    paged.fetch_rotate_scatter(vals, blk.delta_m[:nb], th, w.pairing, np.arange(nb), out, out,
+                               w.out_dtype)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(w, blk, nb):
+    sub = type(blk)(blk.B, blk.src_slots[:nb], blk.dst_slots[:nb], blk.n_valid[:nb],
+                    blk.delta_m[:nb], nb, nb)
+    import copy
+    w1 = copy.copy(w)
+    w1.L = 1
+    return sum(algorithmic_bytes(w1, sub).values()), int(sub.tokens())
+
+
+def cpu_baseline(w, blk, budget_s=15.0):
+    nb = 16
+    k, v = oracle_sample(w, blk, nb)
+    t = time_oracle_step(w, blk, k, v)                 # calibrate
+    nb = int(min(blk.nb, max(16, nb * budget_s / max(t, 1e-3) / 1.1)))
+    k, v = oracle_sample(w, blk, nb)
+    t = time_oracle_step(w, blk, k, v)
+    b, toks = sample_bytes(w, blk, nb)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 of {w.L} layers x {nb} of {blk.nb} blocks ({toks} tokens) of qwen3_8b, "
+                      f"encode FP8 + table + fetch, float64 numpy, one thread; {t:.1f} s",
+            "tokens_per_s": toks / t}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads
+    w = workloads.qwen3_8b()
+    blk = w.blocks[0]
+    nb = args.ref_blocks
+    k, v = oracle_sample(w, blk, nb)
+    for _ in range(args.warmup):
+        time_oracle_step(w, blk, k, v)
+    times = [time_oracle_step(w, blk, k, v) for _ in range(args.steps)]
+    total = sum(times)
+    b, toks = sample_bytes(w, blk, nb)
+    value = b * args.steps / total / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "qwen3_8b (bounded sample per step)", "layers": 1, "blocks": nb},
+        "tokens_per_s": toks * args.steps / total,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": 1,
+                         "sample": f"1 layer x {nb} blocks ({toks} tokens) of qwen3_8b per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a smaller case)")
+    ap.add_argument("--legs", default="device,e2e,cpu", help="comma list of: device, e2e, cpu")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-blocks", type=int, default=16)
+    args = ap.parse_args(argv)
+    args.legs = set(args.legs.split(","))
+    args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+// Internal declarations shared by the kernel translation units and the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/hc.h"
+
+namespace hc {
+
+// One warp owns a "sub-slab": 16 consecutive token rows of one
+// (layer, block, kv, head) slab.  A block of B tokens has B/16 sub-slabs, so a
+// 256-thread CTA (8 warps) always holds whole slabs (B/16 divides 8).
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerWarp = 16;
+
+struct EncodeParams {
+  const void* k;
+  const void* v;
+  int64_t slot_stride;   // elements
+  int64_t layer_stride;  // elements
+  int32_t n_layers, H, B, num_slots, n_blocks, group;
+  const int32_t* src_slots;
+  const int32_t* n_valid;  // may be null
+  uint8_t* codes;
+  void* scales;
+  int32_t* err;
+};
+
+struct FetchParams {
+  const void* codes;
+  const void* scales;
+  const float* table;
+  const int32_t* delta_idx;
+  const int32_t* dst_slots;
+  const int32_t* n_valid;  // may be null
+  void* k;
+  void* v;
+  int64_t slot_stride, layer_stride;
+  int32_t n_layers, H, B, num_slots, n_blocks, n_distinct, group;
+  int32_t* err;
+};
+
+struct TableParams {
+  const int32_t* delta_m;
+  const double* inv_freq;  // may be null: use theta[]
+  float* table;
+  int32_t n_distinct, half;
+  double theta[128];
+};
+
+// Launchers: return the launch's cudaError_t.  `dtype`/`out_dtype` are hc_dtype.
+cudaError_t launch_encode_fp8(int dtype, int d, const EncodeParams& p, cudaStream_t s);
+cudaError_t launch_encode_int4(int dtype, int d, bool scale_f16, const EncodeParams& p,
+                               cudaStream_t s);
+cudaError_t launch_fetch_fp8(int out_dtype, int d, bool half_split, const FetchParams& p,
+                             cudaStream_t s);
+cudaError_t launch_fetch_int4(int out_dtype, int d, bool half_split, bool scale_f16,
+                              const FetchParams& p, cudaStream_t s);
+cudaError_t launch_fetch_raw(int out_dtype, int d, bool half_split, const FetchParams& p,
+                             cudaStream_t s);
+cudaError_t launch_delta_table(const TableParams& p, cudaStream_t s);
+
+// Grid for a kernel with one warp per 16-row sub-slab.
+__host__ __device__ inline int64_t sub_slab_count(int64_t n_layers, int64_t n_blocks, int64_t H, int64_t B) {
+  return n_layers * n_blocks * 2 * H * (B / kRowsPerWarp);
+}
+
+// ---------------------------------------------------------------- device side
+#ifdef __CUDACC__
+
+// Decompose a global sub-slab index into (layer, block, kv, head, sub).
+struct SlabCoord {
+  int64_t slab;  // ((l * n_blocks + j) * 2 + kv) * H + h
+  int32_t l, j, kv, h, sub;
+};
+
+__device__ __forceinline__ SlabCoord slab_coord(int64_t gw, int H, int n_blocks, int wps) {
+  SlabCoord c;
+  c.slab = gw / wps;
+  c.sub = static_cast<int32_t>(gw - c.slab * wps);
+  int64_t r = c.slab;
+  c.h = static_cast<int32_t>(r % H);
+  r /= H;
+  c.kv = static_cast<int32_t>(r & 1);
+  r >>= 1;
+  c.j = static_cast<int32_t>(r % n_blocks);
+  c.l = static_cast<int32_t>(r / n_blocks);
+  return c;
+}
+
+// 8 consecutive elements of a source/destination dtype, kept as raw 16-byte words.
+template <typename T>
+struct Raw8 {
+  static constexpr int kWords = sizeof(T) == 4 ? 2 : 1;
+  uint4 w[kWords];
+};
+
+template <typename T>
+__device__ __forceinline__ Raw8<T> load8_stream(const T* p) {
+  Raw8<T> r;
+#pragma unroll
+  for (int i = 0; i < Raw8<T>::kWords; ++i) r.w[i] = __ldcs(reinterpret_cast<const uint4*>(p) + i);
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ Raw8<T> raw8_zero() {
+  Raw8<T> r;
+#pragma unroll
+  for (int i = 0; i < Raw8<T>::kWords; ++i) r.w[i] = make_uint4(0, 0, 0, 0);
+  return r;
+}
+
+__device__ __forceinline__ float2 u32_to_float2(uint32_t u, const __half*) {
+  __half2 h;
+  memcpy(&h, &u, 4);
+  return __half22float2(h);
+}
+__device__ __forceinline__ float2 u32_to_float2(uint32_t u, const __nv_bfloat16*) {
+  __nv_bfloat162 h;
+  memcpy(&h, &u, 4);
+  return __bfloat1622float2(h);
+}
+
+template <typename T>
+__device__ __forceinline__ void raw8_to_float(const Raw8<T>& r, float (&x)[8]) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      x[4 * i + 0] = __uint_as_float(r.w[i].x);
+      x[4 * i + 1] = __uint_as_float(r.w[i].y);
+      x[4 * i + 2] = __uint_as_float(r.w[i].z);
+      x[4 * i + 3] = __uint_as_float(r.w[i].w);
+    }
+  } else {
+    const uint32_t u[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = u32_to_float2(u[i], static_cast<const T*>(nullptr));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  }
+}
+
+// Largest |x| bit pattern over the 8 elements, as an fp32 value (exact:
+// clearing sign bits and comparing magnitudes as unsigned integers is
+// monotone for finite values).
+template <typename T>
+__device__ __forceinline__ float raw8_absmax(const Raw8<T>& r) {
+  if constexpr (sizeof(T) == 4) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      m = max(m, r.w[i].x & 0x7fffffffu);
+      m = max(m, r.w[i].y & 0x7fffffffu);
+      m = max(m, r.w[i].z & 0x7fffffffu);
+      m = max(m, r.w[i].w & 0x7fffffffu);
+    }
+    return __uint_as_float(m);
+  } else {
+    uint32_t m = __vmaxu2(__vmaxu2(r.w[0].x & 0x7fff7fffu, r.w[0].y & 0x7fff7fffu),
+                          __vmaxu2(r.w[0].z & 0x7fff7fffu, r.w[0].w & 0x7fff7fffu));
+    uint32_t hi = m >> 16, lo = m & 0xffffu;
+    uint32_t b = max(hi, lo);
+    float2 f = u32_to_float2(b, static_cast<const T*>(nullptr));
+    return f.x;
+  }
+}
+
+// Store 8 fp32 values to 8 destination elements, rounding to nearest even.
+__device__ __forceinline__ void store8(float* p, const float (&y)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(y[4], y[5], y[6], y[7]));
+}
+__device__ __forceinline__ void store8(__half* p, const float (&y)[8]) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = __floats2half2_rn(y[2 * i], y[2 * i + 1]);
+    memcpy(&u[i], &h, 4);
+  }
+  __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&y)[8]) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+    memcpy(&u[i], &h, 4);
+  }
+  __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
+}
+
+__device__ __forceinline__ void flag_error(int32_t* err, int bits) {
+  if (bits) atomicOr(err, bits);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace hc

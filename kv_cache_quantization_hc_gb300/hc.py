@@ -1,0 +1,160 @@
+"""ctypes binding of libhc.so: the C-ABI calls under the same names.
+
+Argument marshalling only: every call here converts tensors to device
+addresses, fills the descriptor struct, passes the stream and turns a negative
+status into an exception.  All work runs in the library's CUDA kernels.  If
+libhc.so is missing the first call raises; there is no other code path.
+"""
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libhc.so")
+
+HC_OK, HC_ERR_INVALID_ARG, HC_ERR_UNSUPPORTED, HC_ERR_CUDA = 0, -1, -2, -3
+HC_F32, HC_F16, HC_BF16 = 0, 1, 2
+HC_PAIR_INTERLEAVED, HC_PAIR_HALF_SPLIT = 0, 1
+HC_WIRE_FP8, HC_WIRE_INT4, HC_WIRE_RAW = 0, 1, 2
+HC_DEVERR_SLOT, HC_DEVERR_DELTA, HC_DEVERR_NVALID = 1, 2, 4
+
+DTYPE_NAMES = {"f32": HC_F32, "f16": HC_F16, "bf16": HC_BF16}
+PAIRING_NAMES = {"interleaved": HC_PAIR_INTERLEAVED, "half_split": HC_PAIR_HALF_SPLIT}
+
+
+class HCError(RuntimeError):
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        super().__init__(f"{fn} returned {status_string(status)}" + (f" ({detail})" if detail else ""))
+
+
+class hc_paged_desc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("d_head", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_slots", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("slot_stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64)]
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+
+
+def lib():
+    """Load libhc.so once; raise if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`"
+                " (the CUDA path has no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        desc_p = ctypes.POINTER(hc_paged_desc)
+        L.hc_encode_fp8.argtypes = [_P, _P, desc_p, _P, _P, _I32, _P, _P, _P, _P]
+        L.hc_encode_int4.argtypes = [_P, _P, desc_p, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]
+        L.hc_build_delta_sincos.argtypes = [_P, _I32, _I32, ctypes.c_double, _P, _P, _P]
+        L.hc_fetch_rotate_scatter.argtypes = [_I32, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _P, _P,
+                                              _I32, _P, _P, desc_p, _P, _P]
+        for fn in ("hc_encode_fp8", "hc_encode_int4", "hc_build_delta_sincos",
+                   "hc_fetch_rotate_scatter"):
+            getattr(L, fn).restype = ctypes.c_int
+        L.hc_status_string.argtypes = [_I32]
+        L.hc_status_string.restype = ctypes.c_char_p
+        L.hc_last_cuda_error.argtypes = []
+        L.hc_last_cuda_error.restype = ctypes.c_char_p
+        L.hc_version.argtypes = []
+        L.hc_version.restype = ctypes.c_int32
+        _LIB = L
+    return _LIB
+
+
+# ------------------------------------------------------------- marshalling
+def _ptr(x):
+    """Device/host address of a tensor, an int address, or None (NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    """cudaStream_t of a torch stream; None means torch's current stream."""
+    if isinstance(s, int):
+        return s
+    import torch
+    if s is None:
+        s = torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(fn, status):
+    if status != HC_OK:
+        detail = lib().hc_last_cuda_error().decode() if status == HC_ERR_CUDA else ""
+        raise HCError(fn, status, detail)
+
+
+def status_string(status):
+    return lib().hc_status_string(status).decode()
+
+
+def hc_version():
+    return lib().hc_version()
+
+
+def paged_desc(pool, dtype=None, n_layers=None, layer_stride=None, slot_stride=None):
+    """Descriptor of a pool tensor shaped [L, num_slots, B, H, d] (or
+    [num_slots, B, H, d] for one layer).  Strides are taken from the tensor."""
+    if pool.dim() == 4:
+        pool = pool.unsqueeze(0)
+    L, S, B, H, d = pool.shape
+    if pool.stride(4) != 1 or pool.stride(3) != d or pool.stride(2) != H * d:
+        raise ValueError("each slot must be a contiguous [B, H, d] block")
+    if dtype is None:
+        dtype = {"torch.float32": HC_F32, "torch.float16": HC_F16,
+                 "torch.bfloat16": HC_BF16}[str(pool.dtype)]
+    return hc_paged_desc(n_layers if n_layers is not None else L, H, d, B, S, dtype,
+                         slot_stride if slot_stride is not None else pool.stride(1),
+                         layer_stride if layer_stride is not None else (pool.stride(0) if L > 1 else 0))
+
+
+# ------------------------------------------------------------- the C-ABI calls
+def hc_encode_fp8(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes, scales, err_flag,
+                  stream=None):
+    _check("hc_encode_fp8", lib().hc_encode_fp8(
+        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
+        n_blocks, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
+
+
+def hc_encode_int4(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, group, scale_dtype,
+                   codes, scales, err_flag, stream=None):
+    _check("hc_encode_int4", lib().hc_encode_int4(
+        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
+        n_blocks, group, scale_dtype, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
+
+
+def hc_build_delta_sincos(delta_m, n_distinct, d_head, rope_base, inv_freq, table, stream=None):
+    _check("hc_build_delta_sincos", lib().hc_build_delta_sincos(
+        _ptr(delta_m), n_distinct, d_head, float(rope_base), _ptr(inv_freq), _ptr(table),
+        _stream(stream)))
+
+
+def hc_fetch_rotate_scatter(wire, codes, scales, group, scale_dtype, table, delta_idx, n_distinct,
+                            pairing, dst_slots, n_valid, n_blocks, paged_k, paged_v, desc,
+                            err_flag, stream=None):
+    _check("hc_fetch_rotate_scatter", lib().hc_fetch_rotate_scatter(
+        wire, _ptr(codes), _ptr(scales), group, scale_dtype, _ptr(table), _ptr(delta_idx),
+        n_distinct, pairing, _ptr(dst_slots), _ptr(n_valid), n_blocks, _ptr(paged_k),
+        _ptr(paged_v), ctypes.byref(desc), _ptr(err_flag), _stream(stream)))
+
+
+# ------------------------------------------------------------- buffer shapes
+def wire_shapes(n_layers, n_blocks, H, B, d, wire, group=32):
+    """(codes shape, codes dtype name, scales shape) of a wire buffer, per the
+    layouts in include/hc.h.  RAW codes are in the paged dtype."""
+    if wire == HC_WIRE_FP8:
+        return (n_layers, n_blocks, 2, H, B, d), "u8", (n_layers, n_blocks, 2, H)
+    if wire == HC_WIRE_INT4:
+        return (n_layers, n_blocks, 2, H, B, d // 2), "u8", (n_layers, n_blocks, 2, H, B, d // group)
+    if wire == HC_WIRE_RAW:
+        return (n_layers, n_blocks, 2, H, B, d), "paged", None
+    raise ValueError(wire)

@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads and exports every symbol include/hc.h
+declares; host-side validation answers without touching CUDA (CPU only)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "hc.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_0-9]+\s*\*?\s*(hc_[a-z0-9_]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from kv_cache_quantization_hc_gb300 import build, hc
+    build.build()
+    return hc.lib()
+
+
+def test_header_declares_the_four_calls():
+    names = _declared_functions()
+    for n in ("hc_encode_fp8", "hc_encode_int4", "hc_build_delta_sincos",
+              "hc_fetch_rotate_scatter", "hc_status_string"):
+        assert n in names, names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    from kv_cache_quantization_hc_gb300 import hc
+    assert hc.hc_version() == 1
+    assert hc.status_string(0) == "HC_OK"
+    assert hc.status_string(-1) == "HC_ERR_INVALID_ARG"
+    assert hc.status_string(-2) == "HC_ERR_UNSUPPORTED"
+    assert hc.status_string(-3) == "HC_ERR_CUDA"
+    assert hc.status_string(5) == "HC_UNKNOWN_STATUS"
+    assert lib.hc_last_cuda_error() == b""
+
+
+def test_host_validation_without_cuda(lib):
+    """Every check below returns before any CUDA call (fake addresses)."""
+    from kv_cache_quantization_hc_gb300 import hc
+    A = 1 << 20          # a 16-byte aligned fake address; never dereferenced
+    good = hc.hc_paged_desc(1, 8, 128, 16, 4, hc.HC_BF16, 16 * 8 * 128, 0)
+    L = lib
+    P = ctypes.byref
+    # null paged pointer
+    assert L.hc_encode_fp8(None, A, P(good), A, None, 1, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    # unsupported d_head / block size / group
+    for bad in (hc.hc_paged_desc(1, 8, 96, 16, 4, hc.HC_BF16, 16 * 8 * 96, 0),
+                hc.hc_paged_desc(1, 8, 128, 8, 4, hc.HC_BF16, 8 * 8 * 128, 0)):
+        assert L.hc_encode_fp8(A, A, P(bad), A, None, 1, A, A, A, None) == hc.HC_ERR_UNSUPPORTED
+    assert L.hc_encode_int4(A, A, P(good), A, None, 1, 16, hc.HC_F16, A, A, A, None) == hc.HC_ERR_UNSUPPORTED
+    # misaligned codes, negative block count, unknown dtype, too-small slot stride
+    assert L.hc_encode_fp8(A, A, P(good), A, None, 1, A + 1, A, A, None) == hc.HC_ERR_INVALID_ARG
+    assert L.hc_encode_fp8(A, A, P(good), A, None, -1, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    bad = hc.hc_paged_desc(1, 8, 128, 16, 4, 9, 16 * 8 * 128, 0)
+    assert L.hc_encode_fp8(A, A, P(bad), A, None, 1, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    bad = hc.hc_paged_desc(1, 8, 128, 16, 4, hc.HC_BF16, 100, 0)
+    assert L.hc_encode_fp8(A, A, P(bad), A, None, 1, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    bad = hc.hc_paged_desc(2, 8, 128, 16, 4, hc.HC_BF16, 16 * 8 * 128, 0)   # 2 layers, stride 0
+    assert L.hc_encode_fp8(A, A, P(bad), A, None, 1, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    # fetch: unknown wire / pairing, missing scales, no table rows
+    f = L.hc_fetch_rotate_scatter
+    assert f(7, A, A, 32, hc.HC_F16, A, A, 1, 0, A, None, 1, A, A, P(good), A, None) == hc.HC_ERR_INVALID_ARG
+    assert f(0, A, A, 32, hc.HC_F16, A, A, 1, 5, A, None, 1, A, A, P(good), A, None) == hc.HC_ERR_INVALID_ARG
+    assert f(0, A, None, 32, hc.HC_F16, A, A, 1, 0, A, None, 1, A, A, P(good), A, None) == hc.HC_ERR_INVALID_ARG
+    assert f(0, A, A, 32, hc.HC_F16, A, A, 0, 0, A, None, 1, A, A, P(good), A, None) == hc.HC_ERR_INVALID_ARG
+    assert f(1, A, A, 256, hc.HC_F16, A, A, 1, 0, A, None, 1, A, A, P(good), A, None) == hc.HC_ERR_UNSUPPORTED
+    # table: odd d_head, bad base
+    t = L.hc_build_delta_sincos
+    assert t(A, 1, 127, ctypes.c_double(1e4), None, A, None) == hc.HC_ERR_INVALID_ARG
+    assert t(A, 1, 128, ctypes.c_double(0.0), None, A, None) == hc.HC_ERR_INVALID_ARG
+    assert t(A, -1, 128, ctypes.c_double(1e4), None, A, None) == hc.HC_ERR_INVALID_ARG
+    # zero blocks / rows launch nothing and succeed
+    assert L.hc_encode_fp8(A, A, P(good), A, None, 0, A, A, A, None) == hc.HC_OK
+    assert f(0, A, A, 32, hc.HC_F16, A, A, 0, 0, A, None, 0, A, A, P(good), A, None) == hc.HC_OK
+    assert t(A, 0, 128, ctypes.c_double(1e4), None, A, None) == hc.HC_OK

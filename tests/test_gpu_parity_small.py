@@ -1,0 +1,245 @@
+"""GPU parity on the small workloads and a sweep of shapes, through the C ABI.
+
+Bars (tests/parity.py): codes/scales bit-exact; K within 2e-6 x row max
+(fp32) or 1 ulp (+ that floor) for fp16/bf16; V bit-exact (1 ulp for FP8 into
+16-bit outputs); untouched destination bytes unchanged.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _assert_ok(rep):
+    assert rep["ok"], rep
+
+
+@pytest.mark.parametrize("wire", ["fp8", "int4", "raw"])
+def test_tiny(wire):
+    _assert_ok(parity.run_small_case("tiny", wire))
+
+
+@pytest.mark.parametrize("wire,scale_dtype", [("fp8", "f16"), ("int4", "f16"), ("int4", "f32"),
+                                              ("raw", "f16")])
+def test_gqa_reorder(wire, scale_dtype):
+    rep = parity.run_small_case("gqa_reorder", wire, scale_dtype=scale_dtype)
+    _assert_ok(rep)
+
+
+SWEEP = [
+    # d, B, src, out, pairing, ragged, wire, group, scale
+    (128, 16, "bf16", "bf16", "half_split", False, "fp8", 32, "f16"),
+    (128, 32, "f16", "f16", "interleaved", True, "fp8", 32, "f16"),
+    (128, 64, "bf16", "bf16", "half_split", True, "fp8", 32, "f16"),
+    (128, 128, "f32", "f32", "interleaved", True, "fp8", 32, "f16"),
+    (64, 16, "f16", "f32", "half_split", True, "fp8", 32, "f16"),
+    (64, 64, "f32", "bf16", "interleaved", False, "fp8", 32, "f16"),
+    (128, 16, "bf16", "bf16", "half_split", True, "int4", 32, "f16"),
+    (128, 64, "f16", "f32", "interleaved", True, "int4", 64, "f32"),
+    (128, 32, "f32", "f16", "half_split", False, "int4", 128, "f16"),
+    (64, 128, "bf16", "bf16", "interleaved", True, "int4", 64, "f16"),
+    (64, 16, "f32", "f32", "half_split", True, "int4", 32, "f32"),
+    (128, 64, "bf16", "f32", "half_split", True, "raw", 32, "f16"),
+    (64, 32, "f16", "f16", "interleaved", True, "raw", 32, "f16"),
+]
+
+
+@pytest.mark.parametrize("d,B,src,out,pairing,ragged,wire,group,scale", SWEEP)
+def test_shape_sweep(d, B, src, out, pairing, ragged, wire, group, scale):
+    seed = hash((d, B, src, out, pairing, ragged, wire, group, scale)) % 2 ** 31
+    c = parity.random_case(seed, L=2, H=3, d=d, B=B, nb=7, src_fmt=src, out_fmt=out,
+                           pairing=pairing, ragged=ragged)
+    if wire == "raw":
+        c.src_fmt = out
+        c.src_k, c.src_v = parity.round_to(c.src_k, out), parity.round_to(c.src_v, out)
+    _assert_ok(parity.run_case(c, wire, group=group, scale_dtype=scale))
+
+
+# ---------------------------------------------------------------- adversarial values
+def _midpoint_case(seed, wire):
+    """Slabs whose quotients x/s land within a few fp32 ulps of every E4M3
+    rounding midpoint (FP8) or half-integer (INT4), with a non-trivial scale."""
+    from oracle import fp8
+    r = np.random.default_rng(seed)
+    c = parity.random_case(seed, L=1, H=2, d=128, B=16, nb=4, src_fmt="f32", out_fmt="f32")
+    mags = fp8.e4m3_table()[:0x7E]                   # every finite magnitude below 448
+    if wire == "fp8":
+        targets, amax_q = np.concatenate([(mags[:-1] + mags[1:]) / 2, mags]), 448.0
+    else:
+        targets, amax_q = np.arange(-13, 14) / 2.0, 7.0
+    n = c.B * c.d
+    for slot in c.src_slots:
+        for pool in (c.src_k, c.src_v):
+            for h in range(c.H):
+                s_target = np.float32(np.exp(r.uniform(-6, 6)))
+                x = (r.choice(targets, size=n) * r.choice([-1.0, 1.0], size=n)).astype(np.float32)
+                x = x * s_target
+                walk = r.integers(-3, 4, size=n)     # move up to 3 fp32 ulps either way
+                for _ in range(3):
+                    step = np.sign(walk)
+                    toward = np.where(step > 0, np.float32(np.inf), np.float32(-np.inf))
+                    x = np.where(walk != 0, np.nextafter(x, toward), x)
+                    walk = walk - step
+                x[0] = np.float32(amax_q) * s_target   # pins the slab / group amax
+                if wire == "int4":
+                    x.reshape(c.B, c.d // 32, 32)[:, :, 0] = np.float32(amax_q) * s_target
+                pool[0, slot, :, h, :] = x.astype(np.float64).reshape(c.B, c.d)
+    return c
+
+
+@pytest.mark.parametrize("wire", ["fp8", "int4"])
+@pytest.mark.parametrize("seed", [11, 12])
+def test_midpoint_adversarial(wire, seed):
+    c = _midpoint_case(seed, wire)
+    _assert_ok(parity.run_case(c, wire, scale_dtype="f32"))
+
+
+def test_zero_slab_signed_zero_and_tiny():
+    c = parity.random_case(21, L=1, H=2, d=64, B=16, nb=3, src_fmt="f32", out_fmt="f32")
+    s0 = c.src_slots[0]
+    c.src_k[0, s0] = 0.0                       # all-zero slab: scale 0, codes 0
+    c.src_v[0, s0] = -0.0
+    s1 = c.src_slots[1]
+    c.src_k[0, s1, :, :, :8] = -0.0            # -0 next to non-zeros: 0x80
+    c.src_k[0, s1, :, :, 8:16] = -1e-30        # underflows to -0: 0x80
+    for wire in ("fp8", "int4"):
+        _assert_ok(parity.run_case(c, wire))
+
+
+@pytest.mark.parametrize("fmt,big", [("f16", 65504.0), ("bf16", 3.0e38), ("f32", 3.0e38)])
+def test_large_magnitudes(fmt, big):
+    c = parity.random_case(31, L=1, H=1, d=128, B=16, nb=2, src_fmt=fmt, out_fmt="f32", scale=1.0)
+    c.src_k[0, c.src_slots[0], 3, 0, 5] = parity.round_to(np.array(big), fmt)
+    c.src_v[0, c.src_slots[1], 0, 0, 0] = parity.round_to(np.array(-big), fmt)
+    _assert_ok(parity.run_case(c, "fp8"))
+    _assert_ok(parity.run_case(c, "int4", scale_dtype="f32"))
+
+
+# ---------------------------------------------------------------- error paths
+def _tiny_path(wire="fp8", **over):
+    from kv_cache_quantization_hc_gb300 import path as kvpath
+    c = parity.random_case(41, L=1, H=2, d=64, B=16, nb=4, src_fmt="f32", out_fmt="f32")
+    args = dict(n_layers=1, H=2, d=64, B=16, n_blocks=4, src_slots=c.src_slots,
+                dst_slots=c.dst_slots, n_valid=c.n_valid, delta_m_distinct=np.array([0, 5]),
+                delta_idx=np.array([0, 1, 0, 1]), wire=wire, pairing="interleaved",
+                rope_base=1e4, paged_dtype="f32")
+    args.update(over)
+    p = kvpath.KVPath(**args)
+    src_k = torch.as_tensor(c.src_k, device="cuda").float()
+    src_v = torch.as_tensor(c.src_v, device="cuda").float()
+    return c, p, src_k, src_v
+
+
+@pytest.mark.parametrize("bad,bit", [("slot", 1), ("nvalid", 4)])
+def test_device_error_flag_encode_skips_block(bad, bit):
+    c, p, k, v = _tiny_path()
+    if bad == "slot":
+        p.src_slots[2] = c.num_dst_slots + 100
+    else:
+        p.n_valid = torch.as_tensor(np.array([16, 16, 0, 16], np.int32), device="cuda")
+    p.codes.fill_(0xAB)
+    p.encode(k, v)
+    torch.cuda.synchronize()
+    assert p.error_bits() == bit
+    codes = p.codes.cpu().numpy()
+    assert np.all(codes[:, 2] == 0xAB)               # the bad block was skipped
+    from oracle import paged
+    want, _ = paged.encode_fp8(c.src_k, c.src_v, c.src_slots[[0, 1, 3]])
+    assert np.array_equal(codes[:, [0, 1, 3]], want)
+
+
+@pytest.mark.parametrize("bad,bit", [("slot", 1), ("delta", 2), ("nvalid", 4)])
+def test_device_error_flag_fetch_skips_block(bad, bit):
+    c, p, k, v = _tiny_path()
+    p.encode(k, v)
+    p.build_table()
+    if bad == "slot":
+        p.dst_slots[1] = -1
+    elif bad == "delta":
+        p.delta_idx[1] = 2
+    else:
+        p.n_valid = torch.as_tensor(np.array([16, 17, 16, 16], np.int32), device="cuda")
+    dk = torch.full((1, c.num_dst_slots, 16, 2, 64), parity.SENTINEL, device="cuda")
+    dv = dk.clone()
+    p.fetch(dk, dv)
+    torch.cuda.synchronize()
+    assert p.error_bits() == bit
+    if bad != "slot":
+        assert torch.all(dk[0, c.dst_slots[1]] == parity.SENTINEL)
+        assert torch.all(dv[0, c.dst_slots[1]] == parity.SENTINEL)
+    for j in (0, 2, 3):
+        assert not torch.any(dk[0, c.dst_slots[j]] == parity.SENTINEL)
+
+
+def test_empty_call_is_a_no_op():
+    from kv_cache_quantization_hc_gb300 import hc
+    c, p, k, v = _tiny_path()
+    p.codes.fill_(7)
+    hc.hc_encode_fp8(k, v, hc.paged_desc(k), p.src_slots, None, 0, p.codes, p.scales, p.err)
+    hc.hc_fetch_rotate_scatter(hc.HC_WIRE_FP8, p.codes, p.scales, 32, hc.HC_F16, p.table, p.delta_idx,
+                               0, 0, p.dst_slots, None, 0, k, v, hc.paged_desc(k), p.err)
+    hc.hc_build_delta_sincos(p.delta_m, 0, 64, 1e4, None, p.table)
+    torch.cuda.synchronize()
+    assert p.error_bits() == 0 and torch.all(p.codes == 7)
+
+
+def test_host_argument_errors():
+    from kv_cache_quantization_hc_gb300 import hc
+    c, p, k, v = _tiny_path()
+    desc = hc.paged_desc(k)
+
+    def status(fn, *a):
+        try:
+            fn(*a)
+            return 0
+        except hc.HCError as e:
+            return e.status
+
+    enc = lambda **o: status(hc.hc_encode_fp8, o.get("k", k), v, o.get("desc", desc), p.src_slots,
+                             None, o.get("nb", 4), o.get("codes", p.codes), p.scales, p.err)
+    assert enc(k=None) == hc.HC_ERR_INVALID_ARG
+    assert enc(nb=-1) == hc.HC_ERR_INVALID_ARG
+    assert enc(codes=p.codes.data_ptr() + 1) == hc.HC_ERR_INVALID_ARG
+    bad = hc.hc_paged_desc(1, 2, 96, 16, desc.num_slots, hc.HC_F32, desc.slot_stride, 0)
+    assert enc(desc=bad) == hc.HC_ERR_UNSUPPORTED
+    bad = hc.hc_paged_desc(1, 2, 64, 24, desc.num_slots, hc.HC_F32, desc.slot_stride, 0)
+    assert enc(desc=bad) == hc.HC_ERR_UNSUPPORTED
+    bad = hc.hc_paged_desc(1, 2, 64, 16, desc.num_slots, 7, desc.slot_stride, 0)
+    assert enc(desc=bad) == hc.HC_ERR_INVALID_ARG
+    bad = hc.hc_paged_desc(1, 2, 64, 16, desc.num_slots, hc.HC_F32, 100, 0)
+    assert enc(desc=bad) == hc.HC_ERR_INVALID_ARG
+    assert status(hc.hc_encode_int4, k, v, desc, p.src_slots, None, 4, 48, hc.HC_F16, p.codes,
+                  p.scales, p.err) == hc.HC_ERR_UNSUPPORTED
+    assert status(hc.hc_encode_int4, k, v, desc, p.src_slots, None, 4, 128, hc.HC_F16, p.codes,
+                  p.scales, p.err) == hc.HC_ERR_UNSUPPORTED          # group > d_head
+    assert status(hc.hc_fetch_rotate_scatter, 9, p.codes, p.scales, 32, hc.HC_F16, p.table,
+                  p.delta_idx, 2, 0, p.dst_slots, None, 4, k, v, desc, p.err) == hc.HC_ERR_INVALID_ARG
+    assert status(hc.hc_fetch_rotate_scatter, hc.HC_WIRE_FP8, p.codes, p.scales, 32, hc.HC_F16,
+                  p.table, p.delta_idx, 0, 0, p.dst_slots, None, 4, k, v, desc,
+                  p.err) == hc.HC_ERR_INVALID_ARG                     # n_distinct 0
+    assert status(hc.hc_build_delta_sincos, p.delta_m, 2, 63, 1e4, None, p.table) == hc.HC_ERR_INVALID_ARG
+    assert status(hc.hc_build_delta_sincos, p.delta_m, 2, 64, -1.0, None, p.table) == hc.HC_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert p.error_bits() == 0
+
+
+def test_table_with_inv_freq_override():
+    from kv_cache_quantization_hc_gb300 import hc
+    from oracle import paged
+    th = np.linspace(1.0, 1e-4, 64)
+    dm = np.array([-8192, -1, 0, 3, 4096, 65535], np.int32)
+    t = torch.zeros((6, 64, 2), device="cuda")
+    hc.hc_build_delta_sincos(torch.as_tensor(dm, device="cuda"), 6, 128, 0.0,
+                             torch.as_tensor(th, device="cuda"), t)
+    want = paged.delta_sincos_table(dm, th)
+    got = t.double().cpu().numpy()
+    assert np.all(np.abs(got - want) <= parity.ulp(want, "f32"))
