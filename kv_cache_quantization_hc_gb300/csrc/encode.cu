@@ -19,6 +19,19 @@
 //
 // Reads use the streaming cache hint (each element is read once); codes are
 // written with streaming stores.
+//
+// Quotients without a division per element.  The codes are defined through
+// the IEEE quotient q* = fp32(x / s).  With r = fp32(1/s) and the bracketing
+// multipliers r_lo = fp32(r (1 - 2^-20)), r_hi = fp32(r (1 + 2^-20)), the
+// products q_lo = fp32(x r_lo) and q_hi = fp32(x r_hi) satisfy
+// |q_lo| < |q*| < |q_hi| (three roundings of at most 2^-24 each cannot undo a
+// 2^-20 relative offset; when x/s is so small that fp32 underflows, all three
+// are far below the smallest code step and encode alike).  The quantizer is
+// monotone in |q| for a fixed sign, so when q_lo and q_hi give the same code,
+// that is the code of q*.  Only when they differ (q* within about 2^-20 of a
+// rounding boundary, roughly one element in 10^5) is the IEEE division
+// evaluated.  A scale below the smallest normal fp32 takes the division path
+// for the whole slab, since 1/s may not be representable.
 #include "hc_internal.cuh"
 
 namespace hc {
@@ -30,6 +43,28 @@ struct EncodeGeom {
   static constexpr int kRowsPerPass = 32 / kChunksPerRow;
   static constexpr int kPasses = kRowsPerWarp / kRowsPerPass;
 };
+
+// Bracketing reciprocals of a scale (see the file comment).
+struct Brackets {
+  float lo, hi;
+  bool ok;  // s is a normal fp32, so 1/s and the brackets are accurate
+};
+
+__device__ __forceinline__ Brackets brackets(float s) {
+  Brackets b;
+  const float r = __frcp_rn(s);
+  b.lo = r * (1.0f - 0x1p-20f);
+  b.hi = r * (1.0f + 0x1p-20f);
+  b.ok = s >= 0x1p-126f;
+  return b;
+}
+
+// clamp(round_half_even(q), -7, 7) for |q| < 2^22: adding 1.5 * 2^23 leaves
+// the nearest-even integer in the low mantissa bits (one IEEE rounding).
+__device__ __forceinline__ int int4_round(float q) {
+  const int n = __float_as_int(q + 12582912.0f) - 0x4B400000;
+  return min(7, max(-7, n));
+}
 
 __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
   return static_cast<uint32_t>(
@@ -101,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) k_encode_fp8(EncodeParams p) {
   if (!ss.ok) return;
 
   const float s = __fdiv_rn(amax, 448.0f);
+  const Brackets br = brackets(s);
   uint8_t* out = p.codes + ss.c.slab * static_cast<int64_t>(p.B) * D + ss.chunk * 8;
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
@@ -111,7 +147,10 @@ __global__ void __launch_bounds__(kThreads) k_encode_fp8(EncodeParams p) {
     if (t < ss.nv && s != 0.f) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const uint32_t pr = fp8x2(__fdiv_rn(x[2 * e], s), __fdiv_rn(x[2 * e + 1], s));
+        const float x0 = x[2 * e], x1 = x[2 * e + 1];
+        uint32_t pr = fp8x2(x0 * br.lo, x1 * br.lo);
+        if (pr != fp8x2(x0 * br.hi, x1 * br.hi) || !br.ok)
+          pr = fp8x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
         w[e >> 1] |= pr << (16 * (e & 1));
       }
     }
@@ -157,10 +196,11 @@ __global__ void __launch_bounds__(kThreads) k_encode_int4(EncodeParams p) {
     raw8_to_float(ss.raw[i], x);
     uint32_t packed = 0;
     if (s != 0.f) {
+      const Brackets br = brackets(s);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        int q = __float2int_rn(__fdiv_rn(x[e], s));
-        q = min(7, max(-7, q));
+        int q = int4_round(x[e] * br.lo);
+        if (q != int4_round(x[e] * br.hi) || !br.ok) q = int4_round(__fdiv_rn(x[e], s));
         packed |= (static_cast<uint32_t>(q) & 0xfu) << (4 * e);
       }
     }

@@ -147,6 +147,7 @@ def compare_k(g, e, fmt):
     if fmt != "f32":
         bar = bar + np.maximum(ulp(g, fmt), ulp(e, fmt))
     err = np.abs(g - e)
+    bar = np.broadcast_to(bar, err.shape)
     i = np.unravel_index(np.argmax(err - bar), err.shape) if err.size else ()
     return bool(np.all(err <= bar)), float(err.max(initial=0)), float(bar[i]) if err.size else 0.0
 
