@@ -48,16 +48,17 @@ int check_paged(const hc_paged_desc* d, const void* k, const void* v) {
   return HC_OK;
 }
 
-// The grid has one warp per 16-row sub-slab, 8 warps per CTA; gridDim.x < 2^31.
+// The kernels index sub-slabs with 32-bit arithmetic: fewer than 2^31 per call.
 bool grid_fits(const hc_paged_desc* d, int32_t n_blocks) {
-  const int64_t warps = hc::sub_slab_count(d->n_layers, n_blocks, d->n_kv_heads, d->block_size);
-  return (warps + hc::kWarps - 1) / hc::kWarps < (int64_t{1} << 31);
+  hc::SlabGrid g;
+  return n_blocks == 0 || hc::make_slab_grid(d->n_layers, n_blocks, d->n_kv_heads, d->block_size, &g);
 }
 
 hc::EncodeParams encode_params(const void* k, const void* v, const hc_paged_desc* d,
                                const int32_t* src, const int32_t* nv, int32_t nb, uint8_t* codes,
                                void* scales, int32_t* err, int32_t group) {
   hc::EncodeParams p;
+  hc::make_slab_grid(d->n_layers, nb, d->n_kv_heads, d->block_size, &p.grid);
   p.k = k;
   p.v = v;
   p.slot_stride = d->slot_stride;
@@ -173,6 +174,7 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
   if (n_blocks == 0) return HC_OK;
 
   hc::FetchParams p;
+  hc::make_slab_grid(desc->n_layers, n_blocks, desc->n_kv_heads, desc->block_size, &p.grid);
   p.codes = codes;
   p.scales = scales;
   p.table = table;

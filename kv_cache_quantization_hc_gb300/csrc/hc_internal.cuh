@@ -8,6 +8,7 @@
 #include <cuda_fp8.h>
 
 #include "../../include/hc.h"
+#include "fastdiv.h"
 
 namespace hc {
 
@@ -18,7 +19,22 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerWarp = 16;
 
+// Flat work index -> (layer, block, kv, head, sub-slab).  A call has
+// total = n_layers * n_blocks * 2 * H * wps sub-slabs (wps = block_size / 16),
+// ordered ((layer * n_blocks + block) * 2H + kv * H + head) * wps + sub, so the
+// wire slab index is (layer * n_blocks + block) * 2H + kv * H + head.  The
+// constants are built on the host; total < 2^31 is checked there.
+struct SlabGrid {
+  FastDivmod per_lj;  // 2 * H * wps: sub-slabs per (layer, block)
+  FastDivmod blocks;  // n_blocks
+  FastDivmod heads;   // H
+  uint32_t wps_log2;  // log2(block_size / 16)
+  uint32_t total;     // sub-slabs in the call
+  uint32_t units;     // ceil(total / 8): one unit = the 8 warps of a CTA
+};
+
 struct EncodeParams {
+  SlabGrid grid;
   const void* k;
   const void* v;
   int64_t slot_stride;   // elements
@@ -32,6 +48,7 @@ struct EncodeParams {
 };
 
 struct FetchParams {
+  SlabGrid grid;
   const void* codes;
   const void* scales;
   const float* table;
@@ -65,6 +82,31 @@ cudaError_t launch_fetch_raw(int out_dtype, int d, bool half_split, const FetchP
                              cudaStream_t s);
 cudaError_t launch_delta_table(const TableParams& p, cudaStream_t s);
 
+// SlabGrid for a call; false if the call has 2^31 or more sub-slabs.
+inline bool make_slab_grid(int64_t n_layers, int64_t n_blocks, int64_t H, int64_t B,
+                           SlabGrid* g) {
+  const int64_t wps = B / kRowsPerWarp;
+  const int64_t total = n_layers * n_blocks * 2 * H * wps;
+  if (n_blocks < 1 || total >= (int64_t{1} << 31)) return false;
+  g->per_lj = FastDivmod(static_cast<uint32_t>(2 * H * wps));
+  g->blocks = FastDivmod(static_cast<uint32_t>(n_blocks));
+  g->heads = FastDivmod(static_cast<uint32_t>(H));
+  g->wps_log2 = 0;
+  while ((int64_t{1} << g->wps_log2) < wps) ++g->wps_log2;
+  g->total = static_cast<uint32_t>(total);
+  g->units = static_cast<uint32_t>((total + kWarps - 1) / kWarps);
+  return true;
+}
+
+// Streaming multiprocessors of the current device (152 on GB300 if the query fails).
+inline int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    return n;
+  return 152;
+}
+
 // Grid for a kernel with one warp per 16-row sub-slab.
 __host__ __device__ inline int64_t sub_slab_count(int64_t n_layers, int64_t n_blocks, int64_t H, int64_t B) {
   return n_layers * n_blocks * 2 * H * (B / kRowsPerWarp);
@@ -72,6 +114,27 @@ __host__ __device__ inline int64_t sub_slab_count(int64_t n_layers, int64_t n_bl
 
 // ---------------------------------------------------------------- device side
 #ifdef __CUDACC__
+
+// Position of one warp's sub-slab, from the flat index (see SlabGrid).
+struct Where {
+  int64_t slab;  // wire slab index
+  uint32_t l, j, kv, h, sub;
+  bool active;   // index < total
+};
+
+__device__ __forceinline__ Where locate(const SlabGrid& g, uint32_t gw) {
+  Where w;
+  w.active = gw < g.total;
+  const uint32_t n = w.active ? gw : 0u;
+  uint32_t lj, u, slab_in_lj;
+  g.per_lj.divmod(n, lj, u);
+  g.blocks.divmod(lj, w.l, w.j);
+  slab_in_lj = u >> g.wps_log2;
+  w.sub = u - (slab_in_lj << g.wps_log2);
+  g.heads.divmod(slab_in_lj, w.kv, w.h);
+  w.slab = static_cast<int64_t>(lj) * (2 * g.heads.d) + slab_in_lj;
+  return w;
+}
 
 // Decompose a global sub-slab index into (layer, block, kv, head, sub).
 struct SlabCoord {
@@ -171,6 +234,66 @@ __device__ __forceinline__ float raw8_absmax(const Raw8<T>& r) {
     float2 f = u32_to_float2(b, static_cast<const T*>(nullptr));
     return f.x;
   }
+}
+
+// Running elementwise max of |x| over raw 16-byte words, kept packed:
+// __half2 / __nv_bfloat162 lanes for 16-bit types, one float for fp32.
+template <typename T>
+struct AbsMax;
+template <>
+struct AbsMax<__half> {
+  __half2 m = __float2half2_rn(0.f);
+  __device__ __forceinline__ void add(const Raw8<__half>& r) {
+    const uint4 w = r.w[0];
+    __half2 a, b, c, d;
+    memcpy(&a, &w.x, 4);
+    memcpy(&b, &w.y, 4);
+    memcpy(&c, &w.z, 4);
+    memcpy(&d, &w.w, 4);
+    m = __hmax2(m, __hmax2(__hmax2(__habs2(a), __habs2(b)), __hmax2(__habs2(c), __habs2(d))));
+  }
+  __device__ __forceinline__ float value() const {
+    const float2 f = __half22float2(m);
+    return fmaxf(f.x, f.y);
+  }
+};
+template <>
+struct AbsMax<__nv_bfloat16> {
+  __nv_bfloat162 m = __float2bfloat162_rn(0.f);
+  __device__ __forceinline__ void add(const Raw8<__nv_bfloat16>& r) {
+    const uint4 w = r.w[0];
+    __nv_bfloat162 a, b, c, d;
+    memcpy(&a, &w.x, 4);
+    memcpy(&b, &w.y, 4);
+    memcpy(&c, &w.z, 4);
+    memcpy(&d, &w.w, 4);
+    m = __hmax2(m, __hmax2(__hmax2(__habs2(a), __habs2(b)), __hmax2(__habs2(c), __habs2(d))));
+  }
+  __device__ __forceinline__ float value() const {
+    const float2 f = __bfloat1622float2(m);
+    return fmaxf(f.x, f.y);
+  }
+};
+template <>
+struct AbsMax<float> {
+  float m = 0.f;
+  __device__ __forceinline__ void add(const Raw8<float>& r) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(r.w[i].x)), fabsf(__uint_as_float(r.w[i].y))),
+                         fmaxf(fabsf(__uint_as_float(r.w[i].z)), fabsf(__uint_as_float(r.w[i].w)))));
+    }
+  }
+  __device__ __forceinline__ float value() const { return m; }
+};
+
+// 8 elements as 4 float2 (exact widening).
+template <typename T>
+__device__ __forceinline__ void raw8_to_float2(const Raw8<T>& r, float2 (&x)[4]) {
+  float f[8];
+  raw8_to_float(r, f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = make_float2(f[2 * i], f[2 * i + 1]);
 }
 
 // Store 8 fp32 values to 8 destination elements, rounding to nearest even.
