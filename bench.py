@@ -425,6 +425,118 @@ def run_reference(args):
     }))
 
 
+# ------------------------------------------------------------------ per-layer workloads
+def layered_bytes(w, blk, wire, group=32):
+    """Algorithmic bytes of one layer's encode and fetch for one block size."""
+    T, H, d, NB = blk.tokens(), w.H, w.d, blk.nb
+    kv_elems = 2 * T * H * d
+    src_b = {"f32": 4, "f16": 2, "bf16": 2}[w.src_dtype]
+    out_b = {"f32": 4, "f16": 2, "bf16": 2}[w.out_dtype]
+    if wire == "fp8":
+        wire_b = kv_elems + NB * 2 * H * 4
+    else:  # INT4, fp16 scales; padding rows carry no payload the method needs
+        wire_b = kv_elems // 2 + 2 * T * H * (d // group) * 2
+    n_distinct = len(np.unique(blk.delta_m))
+    enc = kv_elems * src_b + wire_b + NB * 8
+    fet = wire_b + kv_elems * out_b + n_distinct * (d // 2) * 8 + NB * 12
+    return enc, fet
+
+
+def run_layered(args):
+    """Per-layer calls: every layer is encoded (main stream) and then fetched
+    (on a side stream, after an event), as a layer-streamed fetch runs."""
+    import torch
+    import __graft_entry__
+    import workloads
+    from kv_cache_quantization_hc_gb300 import path as kvpath
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+    w = workloads.WORKLOADS[args.workload]()
+    if args.layers:
+        w.L = args.layers
+    wire = "fp8" if args.workload == "llama3_70b" else args.wire
+    main = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device=device)
+    groups = []
+    for blk in w.blocks:
+        p = kvpath.from_blocks(w, blk, wire, device=device, n_layers=1, scale_dtype="f16")
+        src_k = workloads.device_pool(w, blk, range(0, 1), 0, device)
+        src_v = workloads.device_pool(w, blk, range(0, 1), 1, device)
+        shape = (1, blk.num_dst_slots, blk.B, w.H, w.d)
+        dst_k = torch.empty(shape, dtype=workloads.torch_dtype(w.out_dtype), device=device)
+        dst_v = torch.empty_like(dst_k)
+        p.build_table(stream=main)
+        groups.append((blk, p, src_k, src_v, dst_k, dst_v, layered_bytes(w, blk, wire)))
+    evs = []
+
+    def step(record):
+        for layer in range(w.L):
+            for gi, (blk, p, sk, sv, dk, dv, _) in enumerate(groups):
+                e = record[layer][gi] if record else None
+                if e: e[0].record(main)
+                p.encode(sk, sv, stream=main)
+                if e: e[1].record(main)
+                done = torch.cuda.Event()
+                done.record(main)
+                side.wait_event(done)
+                if e: e[2].record(side)
+                p.fetch(dk, dv, stream=side)
+                if e: e[3].record(side)
+        j = torch.cuda.Event()
+        j.record(side)
+        main.wait_event(j)
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize(device)
+    rec = [[[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in groups]
+            for _ in range(w.L)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize(device)
+        start.record(main)
+        for i in range(args.steps):
+            step(rec[i])
+        end.record(main)
+        torch.cuda.synchronize(device)
+    total_s = start.elapsed_time(end) / 1e3
+    if any(g[1].error_bits() for g in groups):
+        raise RuntimeError("device error flag set")
+    enc_t, fet_t = [], []
+    for r in rec:
+        for layer in r:
+            for e in layer:
+                enc_t.append(e[0].elapsed_time(e[1]) / 1e3)
+                fet_t.append(e[2].elapsed_time(e[3]) / 1e3)
+    enc_b = sum(g[6][0] for g in groups) * w.L
+    fet_b = sum(g[6][1] for g in groups) * w.L
+    n_calls = args.steps * w.L * len(groups)
+    step_bytes = enc_b + fet_b
+    tokens = sum(g[0].tokens() for g in groups)
+    peak, peak_kind = measured_peaks()
+    enc_gbs = enc_b * args.steps / sum(enc_t) / 1e9
+    fet_gbs = fet_b * args.steps / sum(fet_t) / 1e9
+    print(json.dumps({
+        "metric": METRIC, "value": step_bytes * args.steps / total_s / 1e9, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.L} layers, per-layer encode (main stream) + fetch "
+                               f"(side stream), wire {wire}, blocks "
+                               + "/".join(f"{g[0].nb}xB{g[0].B}" for g in groups),
+                   "tokens": tokens, "calls_per_step": 2 * w.L * len(groups)},
+        "tokens_per_s": tokens * args.steps / total_s,
+        "kernels": {"encode": {"avg_us_per_call": statistics.mean(enc_t) * 1e6, "gbs": enc_gbs,
+                               "frac": enc_gbs / peak},
+                    "fetch": {"avg_us_per_call": statistics.mean(fet_t) * 1e6, "gbs": fet_gbs,
+                              "frac": fet_gbs / peak}},
+        "peak": peak, "peak_source": peak_kind, "gpu_launches": 2 * n_calls,
+        "clocks": clocks.summary()}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,15 +544,21 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a smaller case)")
+    ap.add_argument("--workload", choices=["qwen3_8b", "llama3_70b", "ragged"], default="qwen3_8b",
+                    help="qwen3_8b: the step the JSON line reports by default; the others time the "
+                         "per-layer calls of the layer-streamed and ragged workloads")
     ap.add_argument("--legs", default="device,e2e,cpu", help="comma list of: device, e2e, cpu")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-blocks", type=int, default=16)
+    ap.add_argument("--wire", choices=["int4", "fp8"], default="int4", help="ragged workload's wire format")
     args = ap.parse_args(argv)
     args.legs = set(args.legs.split(","))
     args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "qwen3_8b":
+        run_layered(args)
     else:
         run_ours(args)
 

@@ -58,19 +58,22 @@ def _lib_matches_host(path):
     return machine == _ELF_MACHINE.get(platform.machine(), -1)
 
 
-def build(force=False, verbose=False, extra_flags=()):
-    """Compile and link libhc.so; returns its path."""
+def build(force=False, verbose=False, extra_flags=(), out_dir=None):
+    """Compile and link libhc.so; returns its path.  ``out_dir`` places the
+    objects and the library elsewhere (a variant built with extra flags)."""
+    build_dir = BUILD if out_dir is None else out_dir
+    lib = LIB if out_dir is None else os.path.join(out_dir, "libhc.so")
     stamp = _stamp(extra_flags)
-    stamp_path = os.path.join(BUILD, "stamp")
-    if not force and _lib_matches_host(LIB) and os.path.exists(stamp_path):
+    stamp_path = os.path.join(build_dir, "stamp")
+    if not force and _lib_matches_host(lib) and os.path.exists(stamp_path):
         with open(stamp_path) as f:
             if f.read().strip() == stamp:
-                return LIB
-    os.makedirs(BUILD, exist_ok=True)
+                return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -81,15 +84,15 @@ def build(force=False, verbose=False, extra_flags=()):
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_path, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

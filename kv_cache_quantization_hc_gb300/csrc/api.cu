@@ -69,6 +69,7 @@ hc::EncodeParams encode_params(const void* k, const void* v, const hc_paged_desc
   p.num_slots = d->num_slots;
   p.n_blocks = nb;
   p.group = group;
+  p.group_log2 = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.src_slots = src;
   p.n_valid = nv;
   p.codes = codes;
@@ -192,6 +193,7 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
   p.n_blocks = n_blocks;
   p.n_distinct = n_distinct;
   p.group = group;
+  p.group_log2 = group == 128 ? 7 : group == 64 ? 6 : 5;
   p.err = err_flag;
   const bool half = pairing == HC_PAIR_HALF_SPLIT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -21,18 +21,28 @@
 // groups lie inside a token row, so INT4 needs no cross-warp step.
 //
 // Quotients without a division per element.  The codes are defined through
-// the IEEE quotient q* = fp32(x / s).  With r = fp32(1/s) and the bracketing
-// multipliers r_lo = fp32(r (1 - 2^-20)), r_hi = fp32(r (1 + 2^-20)), the
-// products q_lo = fp32(x r_lo) and q_hi = fp32(x r_hi) satisfy
+// the IEEE quotient q* = fp32(x / s).
+//
+// FP8 (and INT4 with fp32 sources or fp32 scales): with r = fp32(1/s) and the
+// bracketing multipliers r_lo = fp32(r (1 - 2^-20)), r_hi = fp32(r (1 + 2^-20)),
+// the products q_lo = fp32(x r_lo) and q_hi = fp32(x r_hi) satisfy
 // |q_lo| < |q*| < |q_hi| (three roundings of at most 2^-24 each cannot undo a
 // 2^-20 relative offset; when x/s is so small that fp32 underflows, all three
 // are far below the smallest code step and encode alike).  The quantizer is
 // monotone in |q| for a fixed sign, so when q_lo and q_hi give the same code,
-// that is the code of q*.  Only when they differ (q* within about 2^-20 of a
-// rounding boundary, roughly one element in 10^5) is the IEEE division
-// evaluated, out of line, for those 8 elements.  A scale below the smallest
-// normal fp32 (fp16 for INT4 fp16 scales, where clamping can then matter)
-// takes the division path.  Products are formed two at a time (FMUL2).
+// that is the code of q*.  Where they differ, q* sits at (or within 2^-20 of)
+// a rounding boundary.  With 16-bit sources that is common - a few elements
+// per thousand are exact E4M3 ties, e.g. x = 3/4 amax gives q = 336 - so the
+// main loop only flags the pass, stores the lower-bracket codes, and a
+// deferred step per sub-slab revisits each lane's flagged passes and resolves
+// just the disagreeing elements (an exact FMA-residual test, see
+// fp8_resolve; IEEE division where that test does not apply), re-storing the
+// 8 codes.  A scale below the smallest normal fp32 takes the division path.
+//
+// INT4 with fp16 scales and 16-bit sources: the quotient corrected by its
+// exact residual, checked exhaustively (see int4x8_corrected); no fallback.
+//
+// Products are formed two at a time (FMUL2 / FFMA2).
 //
 // Reads use the streaming cache hint (each element is read once); codes are
 // written with streaming stores.
@@ -70,13 +80,51 @@ __device__ __forceinline__ uint32_t fp8x2(float2 v) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-__device__ __noinline__ uint2 fp8x8_exact(float2 a, float2 b, float2 c, float2 d, float s) {
-  auto q = [s](float2 v) { return fp8x2(make_float2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))); };
-  return make_uint2(q(a) | (q(b) << 16), q(c) | (q(d) << 16));
+__device__ __forceinline__ uint32_t fp8x1(float v) { return fp8x2(make_float2(v, 0.f)) & 0xffu; }
+
+__device__ __noinline__ uint32_t fp8_div1(float x, float s) { return fp8x1(__fdiv_rn(x, s)); }
+
+// Bit k set iff byte k of w is non-zero (k < 4): fold each byte onto its low
+// bit, then gather the four bits with one multiply (no carries reach 24..27).
+__device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t w) {
+  uint32_t t = w | (w >> 4);
+  t |= t >> 2;
+  t |= t >> 1;
+  t &= 0x01010101u;
+  return ((t * 0x01020408u) >> 24) & 0xfu;
+}
+
+// The code of q* = fp32(x/s) for an element whose bracket codes disagree.
+// The brackets straddle exactly one E4M3 rounding boundary mu (they are 2^-19
+// apart, boundaries at least 2^-4), so the answer is the lower code c_lo, the
+// next code c_hi, or - when q* is mu itself - the even one of the two.  For
+// |q| >= 2^-6 (the normal E4M3 range) mu has the form 1.xxx1 * 2^k, and the
+// upper bracket product lies less than 2^4 fp32 ulps above it: clearing its
+// mantissa below bit 19 gives mu.  The residual res = fma(-mu, s, |x|) =
+// |x| - mu s is exact (its magnitude is below 2^-19 |x| and it has at most 29
+// significant bits ending near x's lowest bit minus 5).  q* = mu exactly iff
+// |x/s - mu| <= ulp(mu)/2, i.e. |res| <= s ulp(mu)/2 (mu has few significant
+// bits, so an fp32 tie also rounds to it); otherwise the sign of res gives the
+// side.  Quotients in the E4M3 subnormal range and scales below 2^-90 (where
+// res or s ulp(mu)/2 could leave the normal range) use the IEEE division.
+__device__ __forceinline__ uint32_t fp8_resolve(float xe, float s, float rhi, float s_half_ulp,
+                                                bool resolvable, uint32_t lo_code) {
+  const float ax = fabsf(xe);
+  const float qh = ax * rhi;
+  const uint32_t c_lo = lo_code & 0x7fu;
+  const uint32_t c_hi = c_lo + 1u;
+  if (resolvable && qh >= 0x1p-6f) {
+    const float mu = __uint_as_float(__float_as_uint(qh) & 0xfff80000u);
+    const float res = fmaf(-mu, s, ax);
+    const float thr = __uint_as_float(__float_as_uint(mu) & 0x7f800000u) * s_half_ulp;
+    const uint32_t code = fabsf(res) <= thr ? ((c_lo & 1u) ? c_hi : c_lo) : (res > 0.f ? c_hi : c_lo);
+    return code | (__float_as_uint(xe) >> 31 << 7);
+  }
+  return fp8_div1(xe, s);
 }
 
 // 8 E4M3 codes of x[0..7] / s (see the file comment).
-__device__ __forceinline__ uint2 fp8x8(const float2 (&x)[4], float s, const Brackets& br) {
+__device__ __forceinline__ uint2 fp8x8(const float2 (&x)[4], float s, const Brackets& br, uint2& diff) {
   uint32_t lo[4], hi[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -85,7 +133,7 @@ __device__ __forceinline__ uint2 fp8x8(const float2 (&x)[4], float s, const Brac
   }
   const uint2 wl = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
   const uint2 wh = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-  if (((wl.x ^ wh.x) | (wl.y ^ wh.y)) != 0u || !br.ok) return fp8x8_exact(x[0], x[1], x[2], x[3], s);
+  diff = make_uint2(wl.x ^ wh.x, wl.y ^ wh.y);
   return wl;
 }
 
@@ -101,19 +149,62 @@ __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&b)[8]) {
   return out;
 }
 
-__device__ __noinline__ uint32_t int4x8_exact(float2 a, float2 b, float2 c, float2 d, float s) {
-  const float x[8] = {a.x, a.y, b.x, b.y, c.x, c.y, d.x, d.y};
-  uint32_t out = 0;
+__device__ __forceinline__ uint32_t int4_of(float q) {
+  return static_cast<uint32_t>(min(7, max(-7, __float2int_rn(q)))) & 0xfu;
+}
+
+// INT4 codes for fp16 scales and 16-bit sources: the quotient corrected by its
+// exact residual (Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+//   q1 = fp32(x r),  e = fma(-q1, s, x) (exact),  q = fma(e, r, q1).
+// rint(q) equals rint(fp32(x / s)) for every pair of fp16 values and every
+// pair of bf16 values (x, amax) with |x| <= amax and an fp16 scale of at least
+// 2^-14; this was checked exhaustively against the IEEE division on the GPU
+// (2^32 pairs per format, no mismatch).  On that domain |q| < 7.01, so no
+// clamping is needed.
+__device__ __forceinline__ uint32_t int4x8_corrected(const float2 (&x)[4], float s, float r) {
+  const float2 s2 = make_float2(s, s), r2 = make_float2(r, r);
+  const float2 magic = make_float2(kRintMagic, kRintMagic);
+  uint32_t b[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 q1 = __fmul2_rn(x[e], r2);
+    const float2 res = __ffma2_rn(make_float2(-q1.x, -q1.y), s2, x[e]);
+    const float2 q = __fadd2_rn(__ffma2_rn(res, r2, q1), magic);
+    b[2 * e] = __float_as_uint(q.x);
+    b[2 * e + 1] = __float_as_uint(q.y);
+  }
+  return pack_nibbles(b);
+}
+
+// Where `need` has bit e set, the nibble of clamp(rint(fp32(x_e / s))); called
+// by the whole warp, dividing only at positions some lane needs.
+__device__ __noinline__ uint32_t int4x8_fix(float2 x0, float2 x1, float2 x2, float2 x3, float s,
+                                            uint32_t out, uint32_t need) {
+  const float x[8] = {x0.x, x0.y, x1.x, x1.y, x2.x, x2.y, x3.x, x3.y};
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const int q = min(7, max(-7, __float2int_rn(__fdiv_rn(x[e], s))));
-    out |= (static_cast<uint32_t>(q) & 0xfu) << (4 * e);
+    const bool n = (need >> e) & 1u;
+    if (__any_sync(0xffffffffu, n)) {
+      if (n) out = (out & ~(0xfu << (4 * e))) | (int4_of(__fdiv_rn(x[e], s)) << (4 * e));
+    }
   }
   return out;
 }
 
-// 8 INT4 nibbles of clamp(rint(x[0..7] / s)) (see the file comment).
-__device__ __forceinline__ uint32_t int4x8(const float2 (&x)[4], float s, const Brackets& br) {
+// All 8 nibbles by IEEE division (fp16 scales below the verified domain).
+__device__ __noinline__ uint32_t int4x8_divide(float2 x0, float2 x1, float2 x2, float2 x3, float s) {
+  const float x[8] = {x0.x, x0.y, x1.x, x1.y, x2.x, x2.y, x3.x, x3.y};
+  uint32_t out = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) out |= int4_of(__fdiv_rn(x[e], s)) << (4 * e);
+  return out;
+}
+
+// INT4 codes from the two brackets (fp32 sources or fp32 scales), with the
+// same warp-efficient fallback as FP8.  On the fast path |q| < 7.01.
+__device__ __forceinline__ uint32_t int4x8_brackets(const float2 (&x)[4], float s, const Brackets& br,
+                                                    bool valid) {
   const float2 magic = make_float2(kRintMagic, kRintMagic);
   uint32_t bl[8], bh[8];
 #pragma unroll
@@ -125,11 +216,13 @@ __device__ __forceinline__ uint32_t int4x8(const float2 (&x)[4], float s, const 
     bh[2 * e] = __float_as_uint(qh.x);
     bh[2 * e + 1] = __float_as_uint(qh.y);
   }
-  uint32_t diff = 0;
+  uint32_t out = pack_nibbles(bl);
+  const bool slow = valid && !br.ok;  // per lane: scale too small for the brackets
+  uint32_t need = 0;  // bit e: element e needs the IEEE quotient
 #pragma unroll
-  for (int e = 0; e < 8; ++e) diff |= bl[e] ^ bh[e];
-  if (diff != 0u || !br.ok) return int4x8_exact(x[0], x[1], x[2], x[3], s);
-  return pack_nibbles(bl);
+  for (int e = 0; e < 8; ++e) need |= static_cast<uint32_t>(valid && (slow || bl[e] != bh[e])) << e;
+  if (__any_sync(0xffffffffu, need != 0u)) out = int4x8_fix(x[0], x[1], x[2], x[3], s, out, need);
+  return out;
 }
 
 // Block-table entries a warp needs for one unit.
@@ -199,6 +292,7 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
   const Brackets br = brackets(s, 0x1p-126f);
   uint8_t* out = p.codes + w.slab * static_cast<int64_t>(p.B) * D + chunk * 8;
   const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
+  uint32_t pend = 0;  // bit i: in pass i the brackets disagree somewhere in this lane's chunk
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
     const int t = row0 + i * G::kRowsPerPass;
@@ -206,9 +300,45 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
     if (t < si.nv && s != 0.f) {
       float2 x[4];
       raw8_to_float2(raw[i], x);
-      c = fp8x8(x, s, br);
+      uint2 df;
+      c = fp8x8(x, s, br, df);
+      pend |= static_cast<uint32_t>((df.x | df.y) != 0u || !br.ok) << i;
     }
     __stcs(reinterpret_cast<uint2*>(out + static_cast<int64_t>(t) * D), c);
+  }
+  // Deferred resolution: each lane walks its own flagged passes (usually none
+  // or one), so the warp spends about one short divergent trip per sub-slab.
+  const float s_half_ulp = s * 0x1p-24f;
+  const bool resolvable = br.ok && s >= 0x1p-90f;
+  while (pend != 0u) {
+    const int i = __ffs(static_cast<int>(pend)) - 1;
+    pend &= pend - 1u;
+    Raw8<SrcT> r = raw[0];
+#pragma unroll
+    for (int k = 1; k < G::kPasses; ++k)
+      if (i == k) r = raw[k];
+    float2 x[4];
+    raw8_to_float2(r, x);
+    uint2 df;
+    const uint2 c = fp8x8(x, s, br, df);
+    uint32_t wd[2] = {c.x, c.y};
+    uint32_t todo = br.ok ? (nonzero_bytes4(df.x) | (nonzero_bytes4(df.y) << 4)) : 0xffu;
+    while (todo != 0u) {
+      const int e = __ffs(static_cast<int>(todo)) - 1;
+      todo &= todo - 1u;
+      const float2 xp = e < 2 ? x[0] : e < 4 ? x[1] : e < 6 ? x[2] : x[3];
+      const float xe = (e & 1) ? xp.y : xp.x;
+      const uint32_t sh = 8 * (e & 3);
+      const uint32_t lo_code = (e < 4 ? wd[0] : wd[1]) >> sh;
+      const uint32_t code = br.ok ? fp8_resolve(xe, s, br.hi.x, s_half_ulp, resolvable, lo_code)
+                                  : fp8_div1(xe, s);
+      if (e < 4)
+        wd[0] = (wd[0] & ~(0xffu << sh)) | (code << sh);
+      else
+        wd[1] = (wd[1] & ~(0xffu << sh)) | (code << sh);
+    }
+    const int t = row0 + i * G::kRowsPerPass;
+    __stcs(reinterpret_cast<uint2*>(out + static_cast<int64_t>(t) * D), make_uint2(wd[0], wd[1]));
   }
   if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
 }
@@ -224,12 +354,12 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
     if (lane == 0) flag_error(p.err, bad);
     return;
   }
-  const int lanes_per_group = p.group / 8;  // 4, 8 or 16; groups never straddle rows
-  const int groups_per_row = D / p.group;
+  const int lanes_per_group = 1 << (p.group_log2 - 3);  // 4, 8 or 16; groups never straddle rows
+  const int groups_per_row = D >> p.group_log2;
   uint8_t* out = p.codes + w.slab * static_cast<int64_t>(p.B) * (D / 2) + chunk * 4;
   const int64_t scale_row0 = w.slab * static_cast<int64_t>(p.B) * groups_per_row;
-  const int g = (chunk * 8) / p.group;
-  const bool scale_writer = (chunk % lanes_per_group) == 0;
+  const int g = (chunk * 8) >> p.group_log2;
+  const bool scale_writer = (chunk & (lanes_per_group - 1)) == 0;
   const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
@@ -247,11 +377,17 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
       s = 0.f;
       s16 = __float2half_rn(0.f);
     }
-    uint32_t packed = 0;
-    if (s != 0.f) {
-      float2 x[4];
-      raw8_to_float2(raw[i], x);
-      packed = int4x8(x, s, brackets(s, kScaleF16 ? 0x1p-14f : 0x1p-126f));
+    float2 x[4];
+    raw8_to_float2(raw[i], x);
+    uint32_t packed;
+    if constexpr (kScaleF16 && sizeof(SrcT) == 2) {
+      const float r = __frcp_rn(s);
+      packed = int4x8_corrected(x, s, r);
+      if (!(s >= 0x1p-14f))  // below the verified domain (or s == 0): divide
+        packed = s != 0.f ? int4x8_divide(x[0], x[1], x[2], x[3], s) : 0u;
+    } else {
+      packed = int4x8_brackets(x, s, brackets(s, kScaleF16 ? 0x1p-14f : 0x1p-126f), s != 0.f);
+      if (s == 0.f) packed = 0;
     }
     __stcs(reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(t) * (D / 2)), packed);
     if (scale_writer) {
@@ -324,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_encode(EncodeParams p) {
 template <typename SrcT, int D, int kWire>
 cudaError_t encode_t(const EncodeParams& p, cudaStream_t s) {
   const uint32_t grid = static_cast<uint32_t>(
-      std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * 2));
+      std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * HC_ENCODE_CTAS_PER_SM));
   k_encode<SrcT, D, kWire><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

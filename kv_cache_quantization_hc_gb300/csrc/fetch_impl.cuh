@@ -14,12 +14,19 @@
 // [d/2 + 8q, d/2 + 8q + 8) ("high"), so both pairing conventions keep every
 // rotation pair inside one lane: half-split pairs low[e] with high[e];
 // interleaved pairs (low[2e], low[2e+1]) and (high[2e], high[2e+1]).  d/16
-// lanes cover a row, 512/d rows per pass.  The warp loads its table entries
-// once, issues every pass's code loads before any arithmetic, then converts
-// and stores.  Each store instruction writes 8 output elements per lane;
-// neighbouring lanes write neighbouring 16-byte pieces of one token row, and
-// the 8 warps of a CTA write neighbouring heads.
+// lanes cover a row, 512/d rows per pass.
+//
+// CTAs are persistent (two per SM) and step through units of 8 consecutive
+// sub-slabs, as the encoder does: per warp, the block-table entries of unit
+// i+2 are requested while the codes, scales and rotation-table entries of
+// unit i+1 load (into a second register buffer) and unit i is decoded,
+// rotated and stored.  Each store instruction writes 8 output elements per
+// lane; neighbouring lanes write neighbouring 16-byte pieces of one token
+// row, and the 8 warps of a unit write neighbouring heads.  Products are
+// formed two at a time (FMUL2 / FFMA2).
 #pragma once
+
+#include <algorithm>
 
 #include "hc_internal.cuh"
 
@@ -45,174 +52,278 @@ struct Codes<kFp8, OutT> {
 template <typename OutT>
 struct Codes<kInt4, OutT> {
   uint32_t lo, hi;  // 8 nibbles each
+  float s_lo, s_hi;
 };
 template <typename OutT>
 struct Codes<kRaw, OutT> {
   Raw8<OutT> lo, hi;
 };
 
-__device__ __forceinline__ void fp8x8_to_float(uint2 c, float s, float (&x)[8]) {
+// Everything one warp holds for one sub-slab before decoding it.
+template <int W, typename OutT, int D>
+struct Stage {
+  Codes<W, OutT> cd[FetchGeom<D>::kPasses];
+  float2 cs[4], sn[4];  // rotation table entries (K only): pairs as (cos, cos), (sin, sin)
+  float s_slab;         // FP8 scale
+};
+
+struct Info {
+  int32_t slot, nv, di;
+};
+
+__device__ __forceinline__ Info fetch_info(const FetchParams& p, const Where& w) {
+  Info in{0, 0, 0};
+  if (w.active) {
+    in.slot = __ldg(p.dst_slots + w.j);
+    in.nv = p.n_valid ? __ldg(p.n_valid + w.j) : p.B;
+    in.di = __ldg(p.delta_idx + w.j);
+  }
+  return in;
+}
+
+__device__ __forceinline__ int info_errors(const FetchParams& p, const Info& in) {
+  int bad = 0;
+  if (in.slot < 0 || in.slot >= p.num_slots) bad |= HC_DEVERR_SLOT;
+  if (in.nv < 1 || in.nv > p.B) bad |= HC_DEVERR_NVALID;
+  if (in.di < 0 || in.di >= p.n_distinct) bad |= HC_DEVERR_DELTA;
+  return bad;
+}
+
+__device__ __forceinline__ void fp8x8_to_float2(uint2 c, float s, float2 (&x)[4]) {
   const uint32_t w[2] = {c.x, c.y};
+  const float2 s2 = make_float2(s, s);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>(w[i >> 1] >> (16 * (i & 1)));
     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
     __half2 h;
     memcpy(&h, &hr, 4);
-    const float2 f = __half22float2(h);  // exact: E4M3 values are fp16 values
-    x[2 * i] = f.x * s;                  // one fp32 rounding of the exact product
-    x[2 * i + 1] = f.y * s;
+    x[i] = __fmul2_rn(__half22float2(h), s2);  // exact widening, then one fp32 rounding
   }
 }
 
-__device__ __forceinline__ void int4x8_to_float(uint32_t c, float s, float (&x)[8]) {
+// 8 nibbles -> 8 floats code * s.  Biasing every nibble by 8 makes it the
+// unsigned value code + 8 in [1, 15]; placed in the low byte of the fp32
+// pattern of 2^23 it reads as 2^23 + code + 8, so one subtraction of 2^23 + 8
+// gives the code exactly, and one multiply by s the exact product (|code| <= 7
+// times a scale of at most 24 significant bits).
+__device__ __forceinline__ void int4x8_to_float2(uint32_t c, float s, float2 (&x)[4]) {
+  const uint32_t b = c ^ 0x88888888u;
+  const uint32_t even = b & 0x0f0f0f0fu;         // byte i: element 2i
+  const uint32_t odd = (b >> 4) & 0x0f0f0f0fu;   // byte i: element 2i+1
+  const float2 s2 = make_float2(s, s);
+  const float2 off = make_float2(-8388616.0f, -8388616.0f);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int v = static_cast<int32_t>(c << (28 - 4 * e)) >> 28;  // sign-extend nibble e
-    x[e] = static_cast<float>(v) * s;  // exact: |v| <= 7 times a scale of <= 24 bits
+  for (int i = 0; i < 4; ++i) {
+    const float2 m = make_float2(__uint_as_float(__byte_perm(even, 0x4B000000u, 0x7540 + i)),
+                                 __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7540 + i)));
+    x[i] = __fmul2_rn(__fadd2_rn(m, off), s2);
   }
 }
 
-template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16>
-__global__ void __launch_bounds__(kThreads) k_fetch(FetchParams p) {
+template <typename T>
+__device__ __forceinline__ void raw8_to_f2(const Raw8<T>& r, float2 (&x)[4]) {
+  raw8_to_float2(r, x);
+}
+
+template <int W, typename OutT, int D, bool kHalfSplit, bool kScaleF16>
+__device__ __forceinline__ void load_stage(const FetchParams& p, const Where& w, const Info& in,
+                                           int q, int r, Stage<W, OutT, D>& st) {
   using G = FetchGeom<D>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (gw >= sub_slab_count(p.n_layers, p.n_blocks, p.H, p.B)) return;
-  const SlabCoord c = slab_coord(gw, p.H, p.n_blocks, p.B / kRowsPerWarp);
-
-  const int32_t slot = __ldg(p.dst_slots + c.j);
-  const int32_t nv = p.n_valid ? __ldg(p.n_valid + c.j) : p.B;
-  const int32_t di = __ldg(p.delta_idx + c.j);
-  {
-    int bad = 0;
-    if (slot < 0 || slot >= p.num_slots) bad |= HC_DEVERR_SLOT;
-    if (nv < 1 || nv > p.B) bad |= HC_DEVERR_NVALID;
-    if (di < 0 || di >= p.n_distinct) bad |= HC_DEVERR_DELTA;
-    if (bad) {
-      if (lane == 0) flag_error(p.err, bad);
-      return;
-    }
-  }
-  const int row0 = c.sub * kRowsPerWarp;
-  if (row0 >= nv) return;  // the whole sub-slab is padding
-
-  const int q = lane % G::kLanesPerRow;
-  const int r = lane / G::kLanesPerRow;
-  const int c_lo = 8 * q;
-  const int c_hi = D / 2 + 8 * q;
-
-  // ---- rotation table entries (K only; warp-uniform branch)
-  float cs[8], sn[8];
-  const bool is_k = c.kv == 0;
-  if (is_k) {
-    const float4* tab = reinterpret_cast<const float4*>(p.table + static_cast<int64_t>(di) * D);
-    // float4 k of a row holds pairs 2k and 2k+1 as (c, s, c, s)
+  const bool ok = w.active && info_errors(p, in) == 0;
+  const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + r;
+  const int64_t slab_rows = w.slab * static_cast<int64_t>(p.B);
+  const int c_lo = 8 * q, c_hi = D / 2 + 8 * q;
+  if (ok && w.kv == 0) {
+    const float4* tab = reinterpret_cast<const float4*>(p.table + static_cast<int64_t>(in.di) * D);
+    // float4 k of a table row holds pairs 2k and 2k+1 as (c, s, c, s)
     float4 t4[4];
     if (kHalfSplit) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) t4[i] = __ldg(tab + 4 * q + i);        // pairs 8q .. 8q+7
+      for (int i = 0; i < 4; ++i) t4[i] = __ldg(tab + 4 * q + i);  // pairs 8q .. 8q+7
     } else {
-      t4[0] = __ldg(tab + 2 * q);                                          // pairs 4q .. 4q+3
+      t4[0] = __ldg(tab + 2 * q);                                    // pairs 4q .. 4q+3
       t4[1] = __ldg(tab + 2 * q + 1);
-      t4[2] = __ldg(tab + D / 8 + 2 * q);                                  // pairs d/4+4q ..
+      t4[2] = __ldg(tab + D / 8 + 2 * q);                            // pairs d/4+4q ..
       t4[3] = __ldg(tab + D / 8 + 2 * q + 1);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      cs[2 * i] = t4[i].x;
-      sn[2 * i] = t4[i].y;
-      cs[2 * i + 1] = t4[i].z;
-      sn[2 * i + 1] = t4[i].w;
+      st.cs[i] = make_float2(t4[i].x, t4[i].z);
+      st.sn[i] = make_float2(t4[i].y, t4[i].w);
     }
   }
-
-  // ---- load every pass's codes (and scales) first
-  Codes<W, OutT> cd[G::kPasses];
-  float sc_lo[G::kPasses], sc_hi[G::kPasses];
-  float s_slab = 1.f;
-  const int64_t slab_rows = c.slab * static_cast<int64_t>(p.B);
-  if (W == kFp8) s_slab = __ldg(static_cast<const float*>(p.scales) + c.slab);
+  if (W == kFp8) st.s_slab = ok ? __ldg(static_cast<const float*>(p.scales) + w.slab) : 0.f;
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
-    const int t = row0 + r + i * G::kRowsPerPass;
-    const bool valid = t < nv;
+    const int t = row0 + i * G::kRowsPerPass;
+    const bool valid = ok && t < in.nv;
     const int64_t row = slab_rows + t;
     if constexpr (W == kFp8) {
       const uint8_t* b = static_cast<const uint8_t*>(p.codes) + row * D;
-      cd[i].lo = valid ? __ldcs(reinterpret_cast<const uint2*>(b + c_lo)) : make_uint2(0, 0);
-      cd[i].hi = valid ? __ldcs(reinterpret_cast<const uint2*>(b + c_hi)) : make_uint2(0, 0);
+      st.cd[i].lo = valid ? __ldcs(reinterpret_cast<const uint2*>(b + c_lo)) : make_uint2(0, 0);
+      st.cd[i].hi = valid ? __ldcs(reinterpret_cast<const uint2*>(b + c_hi)) : make_uint2(0, 0);
     } else if constexpr (W == kInt4) {
       const uint8_t* b = static_cast<const uint8_t*>(p.codes) + row * (D / 2);
-      cd[i].lo = valid ? __ldcs(reinterpret_cast<const unsigned int*>(b + c_lo / 2)) : 0u;
-      cd[i].hi = valid ? __ldcs(reinterpret_cast<const unsigned int*>(b + c_hi / 2)) : 0u;
-      const int gpr = D / p.group;
-      const int64_t sb = row * gpr;
+      st.cd[i].lo = valid ? __ldcs(reinterpret_cast<const unsigned int*>(b + c_lo / 2)) : 0u;
+      st.cd[i].hi = valid ? __ldcs(reinterpret_cast<const unsigned int*>(b + c_hi / 2)) : 0u;
+      const int64_t sb = row * (D >> p.group_log2);
+      const int g_lo = c_lo >> p.group_log2, g_hi = c_hi >> p.group_log2;
       if (kScaleF16) {
         const __half* S = static_cast<const __half*>(p.scales);
-        sc_lo[i] = valid ? __half2float(__ldg(S + sb + c_lo / p.group)) : 0.f;
-        sc_hi[i] = valid ? __half2float(__ldg(S + sb + c_hi / p.group)) : 0.f;
+        st.cd[i].s_lo = valid ? __half2float(__ldg(S + sb + g_lo)) : 0.f;
+        st.cd[i].s_hi = valid ? __half2float(__ldg(S + sb + g_hi)) : 0.f;
       } else {
         const float* S = static_cast<const float*>(p.scales);
-        sc_lo[i] = valid ? __ldg(S + sb + c_lo / p.group) : 0.f;
-        sc_hi[i] = valid ? __ldg(S + sb + c_hi / p.group) : 0.f;
+        st.cd[i].s_lo = valid ? __ldg(S + sb + g_lo) : 0.f;
+        st.cd[i].s_hi = valid ? __ldg(S + sb + g_hi) : 0.f;
       }
     } else {
       const OutT* b = static_cast<const OutT*>(p.codes) + row * D;
-      cd[i].lo = valid ? load8_stream(b + c_lo) : raw8_zero<OutT>();
-      cd[i].hi = valid ? load8_stream(b + c_hi) : raw8_zero<OutT>();
+      st.cd[i].lo = valid ? load8_stream(b + c_lo) : raw8_zero<OutT>();
+      st.cd[i].hi = valid ? load8_stream(b + c_hi) : raw8_zero<OutT>();
     }
   }
+}
 
-  OutT* dst = static_cast<OutT*>(is_k ? p.k : p.v) + c.l * p.layer_stride +
-              static_cast<int64_t>(slot) * p.slot_stride + c.h * D;
+// (x1, x2) -> (x1 c - x2 s, x1 s + x2 c) for two pairs at once.
+__device__ __forceinline__ void rotate2(float2& x1, float2& x2, float2 c, float2 s) {
+  const float2 t = __fmul2_rn(x2, s);
+  const float2 u = __fmul2_rn(x2, c);
+  const float2 y1 = __ffma2_rn(x1, c, make_float2(-t.x, -t.y));
+  const float2 y2 = __ffma2_rn(x1, s, u);
+  x1 = y1;
+  x2 = y2;
+}
+
+__device__ __forceinline__ void store8_f2(float* p, const float2 (&y)[4]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(y[0].x, y[0].y, y[1].x, y[1].y));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(y[2].x, y[2].y, y[3].x, y[3].y));
+}
+__device__ __forceinline__ void store8_f2(__half* p, const float2 (&y)[4]) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __float22half2_rn(y[i]);
+    memcpy(&u[i], &h, 4);
+  }
+  __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
+}
+__device__ __forceinline__ void store8_f2(__nv_bfloat16* p, const float2 (&y)[4]) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(y[i]);
+    memcpy(&u[i], &h, 4);
+  }
+  __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
+}
+
+template <int W, typename OutT, int D, bool kHalfSplit, bool kScaleF16>
+__device__ __forceinline__ void process_stage(const FetchParams& p, const Where& w, const Info& in,
+                                              int q, int r, int lane,
+                                              const Stage<W, OutT, D>& st) {
+  using G = FetchGeom<D>;
+  if (!w.active) return;
+  const int bad = info_errors(p, in);
+  if (bad) {
+    if (lane == 0) flag_error(p.err, bad);
+    return;
+  }
+  const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + r;
+  const int c_lo = 8 * q, c_hi = D / 2 + 8 * q;
+  OutT* dst = static_cast<OutT*>(w.kv == 0 ? p.k : p.v) +
+              static_cast<int64_t>(w.l) * p.layer_stride +
+              static_cast<int64_t>(in.slot) * p.slot_stride + w.h * D;
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
-    const int t = row0 + r + i * G::kRowsPerPass;
-    if (t >= nv) continue;
-    float lo[8], hi[8];
+    const int t = row0 + i * G::kRowsPerPass;
+    if (t >= in.nv) continue;
+    float2 lo[4], hi[4];
     if constexpr (W == kFp8) {
-      fp8x8_to_float(cd[i].lo, s_slab, lo);
-      fp8x8_to_float(cd[i].hi, s_slab, hi);
+      fp8x8_to_float2(st.cd[i].lo, st.s_slab, lo);
+      fp8x8_to_float2(st.cd[i].hi, st.s_slab, hi);
     } else if constexpr (W == kInt4) {
-      int4x8_to_float(cd[i].lo, sc_lo[i], lo);
-      int4x8_to_float(cd[i].hi, sc_hi[i], hi);
+      int4x8_to_float2(st.cd[i].lo, st.cd[i].s_lo, lo);
+      int4x8_to_float2(st.cd[i].hi, st.cd[i].s_hi, hi);
     } else {
-      raw8_to_float(cd[i].lo, lo);
-      raw8_to_float(cd[i].hi, hi);
+      raw8_to_f2(st.cd[i].lo, lo);
+      raw8_to_f2(st.cd[i].hi, hi);
     }
-    if (is_k) {
+    if (w.kv == 0) {
       if (kHalfSplit) {
+        // pairs (low[e], high[e]) with table entry 8q + e
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float x1 = lo[e], x2 = hi[e];
-          lo[e] = x1 * cs[e] - x2 * sn[e];
-          hi[e] = x1 * sn[e] + x2 * cs[e];
-        }
+        for (int k = 0; k < 4; ++k) rotate2(lo[k], hi[k], st.cs[k], st.sn[k]);
       } else {
+        // pairs (low[2e], low[2e+1]) -> entry 4q + e; (high[2e], high[2e+1]) -> d/4 + 4q + e
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float x1 = lo[2 * e], x2 = lo[2 * e + 1];
-          lo[2 * e] = x1 * cs[e] - x2 * sn[e];
-          lo[2 * e + 1] = x1 * sn[e] + x2 * cs[e];
-          x1 = hi[2 * e];
-          x2 = hi[2 * e + 1];
-          hi[2 * e] = x1 * cs[4 + e] - x2 * sn[4 + e];
-          hi[2 * e + 1] = x1 * sn[4 + e] + x2 * cs[4 + e];
+        for (int k = 0; k < 2; ++k) {
+          float2 a1 = make_float2(lo[2 * k].x, lo[2 * k + 1].x);
+          float2 a2 = make_float2(lo[2 * k].y, lo[2 * k + 1].y);
+          rotate2(a1, a2, st.cs[k], st.sn[k]);
+          lo[2 * k] = make_float2(a1.x, a2.x);
+          lo[2 * k + 1] = make_float2(a1.y, a2.y);
+          float2 b1 = make_float2(hi[2 * k].x, hi[2 * k + 1].x);
+          float2 b2 = make_float2(hi[2 * k].y, hi[2 * k + 1].y);
+          rotate2(b1, b2, st.cs[2 + k], st.sn[2 + k]);
+          hi[2 * k] = make_float2(b1.x, b2.x);
+          hi[2 * k + 1] = make_float2(b1.y, b2.y);
         }
       }
     }
     OutT* o = dst + static_cast<int64_t>(t) * p.H * D;
-    store8(o + c_lo, lo);
-    store8(o + c_hi, hi);
+    store8_f2(o + c_lo, lo);
+    store8_f2(o + c_hi, hi);
+  }
+}
+
+template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16>
+__global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchParams p) {
+  using St = Stage<W, OutT, D>;
+  constexpr bool kDoubleBuffer = W != kRaw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = lane % FetchGeom<D>::kLanesPerRow, r = lane / FetchGeom<D>::kLanesPerRow;
+  const uint32_t stride = gridDim.x;
+  uint32_t c = blockIdx.x;
+  if (c >= p.grid.units) return;
+  Where w0 = locate(p.grid, c * kWarps + warp);
+  Info i0 = fetch_info(p, w0);
+  if constexpr (kDoubleBuffer) {
+    Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
+    Info i1 = fetch_info(p, w1);
+    St cur;
+    load_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, cur);
+    for (; c < p.grid.units; c += stride) {
+      const Where w2 = locate(p.grid, (c + 2 * stride) * kWarps + warp);
+      const Info i2 = fetch_info(p, w2);
+      St nxt;
+      load_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w1, i1, q, r, nxt);
+      process_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, lane, cur);
+      w0 = w1;
+      i0 = i1;
+      w1 = w2;
+      i1 = i2;
+      cur = nxt;
+    }
+  } else {
+    for (; c < p.grid.units; c += stride) {
+      const Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
+      const Info i1 = fetch_info(p, w1);
+      St cur;
+      load_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, cur);
+      process_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, lane, cur);
+      w0 = w1;
+      i0 = i1;
+    }
   }
 }
 
 template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16>
 cudaError_t launch_t(const FetchParams& p, cudaStream_t s) {
-  const int64_t warps = sub_slab_count(p.n_layers, p.n_blocks, p.H, p.B);
-  const int64_t grid = (warps + kWarps - 1) / kWarps;
-  k_fetch<OutT, D, W, kHalfSplit, kScaleF16><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+  const uint32_t grid = static_cast<uint32_t>(
+      std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * HC_FETCH_CTAS_PER_SM));
+  k_fetch<OutT, D, W, kHalfSplit, kScaleF16><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

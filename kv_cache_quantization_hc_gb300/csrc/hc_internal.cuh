@@ -7,7 +7,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
-#include "../../include/hc.h"
+#include "hc.h"
 #include "fastdiv.h"
 
 namespace hc {
@@ -16,6 +16,18 @@ namespace hc {
 // (layer, block, kv, head) slab.  A block of B tokens has B/16 sub-slabs, so a
 // 256-thread CTA (8 warps) always holds whole slabs (B/16 divides 8).
 constexpr int kThreads = 256;
+
+// Launch shape: persistent CTAs per SM for the encode and fetch kernels, and
+// the occupancy the register budget is sized for.
+#ifndef HC_ENCODE_CTAS_PER_SM
+#define HC_ENCODE_CTAS_PER_SM 2
+#endif
+#ifndef HC_FETCH_CTAS_PER_SM
+#define HC_FETCH_CTAS_PER_SM 2
+#endif
+#ifndef HC_FETCH_MIN_BLOCKS
+#define HC_FETCH_MIN_BLOCKS 2
+#endif
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerWarp = 16;
 
@@ -39,7 +51,7 @@ struct EncodeParams {
   const void* v;
   int64_t slot_stride;   // elements
   int64_t layer_stride;  // elements
-  int32_t n_layers, H, B, num_slots, n_blocks, group;
+  int32_t n_layers, H, B, num_slots, n_blocks, group, group_log2;
   const int32_t* src_slots;
   const int32_t* n_valid;  // may be null
   uint8_t* codes;
@@ -58,7 +70,7 @@ struct FetchParams {
   void* k;
   void* v;
   int64_t slot_stride, layer_stride;
-  int32_t n_layers, H, B, num_slots, n_blocks, n_distinct, group;
+  int32_t n_layers, H, B, num_slots, n_blocks, n_distinct, group, group_log2;
   int32_t* err;
 };
 

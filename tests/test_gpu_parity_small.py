@@ -243,3 +243,34 @@ def test_table_with_inv_freq_override():
     want = paged.delta_sincos_table(dm, th)
     got = t.double().cpu().numpy()
     assert np.all(np.abs(got - want) <= parity.ulp(want, "f32"))
+
+
+def _tie_case(fmt, seed):
+    """Slabs whose amax sweeps the format's mantissas and whose elements sweep
+    all mantissas over several binades: with 16-bit values many quotients
+    x/s land exactly on E4M3 midpoints (e.g. x = 3/4 amax -> 336)."""
+    from oracle.numerics import FORMATS
+    p_bits = FORMATS[fmt][0] - 1
+    r = np.random.default_rng(seed)
+    H, d, B = 1, 128, 16
+    mant = np.arange(1 << p_bits)
+    amax_m = mant if fmt == "bf16" else r.choice(mant, 128, replace=False)
+    nb = len(amax_m)
+    c = parity.random_case(seed, L=1, H=H, d=d, B=B, nb=nb, src_fmt=fmt, out_fmt="f32", extra_slots=0)
+    for j, m in enumerate(amax_m):
+        amax = (1.0 + m / (1 << p_bits)) * 2.0 ** int(r.integers(-3, 4))
+        xs_m = r.choice(mant, B * d)
+        xs = (1.0 + xs_m / (1 << p_bits)) * amax / 2.0 ** r.integers(0, 9, B * d)
+        xs = parity.round_to(np.minimum(xs, amax) * r.choice([-1.0, 1.0], B * d), fmt)
+        xs[0] = amax
+        for pool in (c.src_k, c.src_v):
+            pool[0, c.src_slots[j], :, 0, :] = xs.reshape(B, d)
+    return c
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_exact_ties_16bit(fmt):
+    c = _tie_case(fmt, 51)
+    _assert_ok(parity.run_case(c, "fp8"))
+    _assert_ok(parity.run_case(c, "int4", scale_dtype="f16"))
+    _assert_ok(parity.run_case(c, "int4", scale_dtype="f32"))
