@@ -16,11 +16,12 @@
 // interleaved pairs (low[2e], low[2e+1]) and (high[2e], high[2e+1]).  d/16
 // lanes cover a row, 512/d rows per pass.
 //
-// CTAs are persistent (two per SM) and step through units of 8 consecutive
-// sub-slabs, as the encoder does: per warp, the block-table entries of unit
-// i+2 are requested while the codes, scales and rotation-table entries of
-// unit i+1 load (into a second register buffer) and unit i is decoded,
-// rotated and stored.  Each store instruction writes 8 output elements per
+// A CTA covers a unit of 8 consecutive sub-slabs; by default there is one
+// unit per CTA and 4 CTAs per SM (the register budget is sized for that), as
+// this write-heavy kernel gains more from resident warps than from software
+// pipelining.  The same code runs persistent CTAs that step through units
+// with a per-warp prefetch of the next unit when built with
+// HC_FETCH_CTAS_PER_SM / HC_FETCH_DOUBLE_BUFFER (see hc_internal.cuh).  Each store instruction writes 8 output elements per
 // lane; neighbouring lanes write neighbouring 16-byte pieces of one token
 // row, and the 8 warps of a unit write neighbouring heads.  Products are
 // formed two at a time (FMUL2 / FFMA2).
@@ -281,7 +282,7 @@ __device__ __forceinline__ void process_stage(const FetchParams& p, const Where&
 template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16>
 __global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchParams p) {
   using St = Stage<W, OutT, D>;
-  constexpr bool kDoubleBuffer = W != kRaw;
+  constexpr bool kDoubleBuffer = HC_FETCH_DOUBLE_BUFFER && W != kRaw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = lane % FetchGeom<D>::kLanesPerRow, r = lane / FetchGeom<D>::kLanesPerRow;
   const uint32_t stride = gridDim.x;

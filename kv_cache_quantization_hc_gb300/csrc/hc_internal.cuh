@@ -17,16 +17,20 @@ namespace hc {
 // 256-thread CTA (8 warps) always holds whole slabs (B/16 divides 8).
 constexpr int kThreads = 256;
 
-// Launch shape: persistent CTAs per SM for the encode and fetch kernels, and
-// the occupancy the register budget is sized for.
-#ifndef HC_ENCODE_CTAS_PER_SM
-#define HC_ENCODE_CTAS_PER_SM 2
-#endif
+// Fetch launch shape.  CTAS_PER_SM caps the grid at that many CTAs per SM
+// (the CTAs then loop over units); the default large value gives one unit per
+// CTA.  MIN_BLOCKS is the occupancy the register budget is sized for, and
+// DOUBLE_BUFFER whether a warp loads its next unit while it computes the
+// current one.  Measured on GB300, this write-heavy kernel is fastest with one
+// unit per CTA at 4 CTAs/SM.  (The encoder picks its shape per call.)
 #ifndef HC_FETCH_CTAS_PER_SM
-#define HC_FETCH_CTAS_PER_SM 2
+#define HC_FETCH_CTAS_PER_SM (1 << 20)
 #endif
 #ifndef HC_FETCH_MIN_BLOCKS
-#define HC_FETCH_MIN_BLOCKS 2
+#define HC_FETCH_MIN_BLOCKS 4
+#endif
+#ifndef HC_FETCH_DOUBLE_BUFFER
+#define HC_FETCH_DOUBLE_BUFFER 0
 #endif
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerWarp = 16;
