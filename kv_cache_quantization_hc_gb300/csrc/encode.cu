@@ -142,11 +142,29 @@ __device__ __forceinline__ uint2 fp8x8(const float2 (&x)[4], float s, const Brac
 // four bits are the 4-bit two's complement.
 constexpr float kRintMagic = 12582912.0f;
 
+// Low nibbles of b[0..7] packed, element 2k in the low half of byte k.
 __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&b)[8]) {
-  uint32_t out = 0;
+  uint32_t p[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) out |= (b[e] & 0xfu) << (4 * e);
-  return out;
+  for (int k = 0; k < 4; ++k) p[k] = (b[2 * k] & 0xfu) | ((b[2 * k + 1] << 4) & 0xf0u);
+  return __byte_perm(__byte_perm(p[0], p[1], 0x0040), __byte_perm(p[2], p[3], 0x0040), 0x5410);
+}
+
+// fp32(a / 7) for every non-negative finite fp32 a, without a division: the
+// product with fp32(1/7) is corrected by its exact residual (Markstein's
+// correction, as in int4x8_corrected).  Checked against the IEEE division on
+// the GPU for all 2^31 non-negative finite fp32 values: no mismatch.
+__device__ __forceinline__ float div7(float a) {
+  const float r7 = 0.142857149f;  // fp32(1/7)
+  const float q1 = a * r7;
+  return fmaf(fmaf(-q1, 7.0f, a), r7, q1);
+}
+
+// The hardware reciprocal approximation (at most 1 ulp of error).
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t int4_of(float q) {
@@ -156,20 +174,21 @@ __device__ __forceinline__ uint32_t int4_of(float q) {
 // INT4 codes for fp16 scales and 16-bit sources: the quotient corrected by its
 // exact residual (Markstein, "Computation of elementary functions on the IBM
 // RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
-//   q1 = fp32(x r),  e = fma(-q1, s, x) (exact),  q = fma(e, r, q1).
-// rint(q) equals rint(fp32(x / s)) for every pair of fp16 values and every
-// pair of bf16 values (x, amax) with |x| <= amax and an fp16 scale of at least
-// 2^-14; this was checked exhaustively against the IEEE division on the GPU
-// (2^32 pairs per format, no mismatch).  On that domain |q| < 7.01, so no
-// clamping is needed.
+//   q1 = fp32(x r),  e = fma(-q1, s, x) (exact),  q = fma(e, r, q1),
+// with r the hardware reciprocal approximation of s.  rint(q) equals
+// rint(fp32(x / s)) for every pair of fp16 values and every pair of bf16
+// values (x, amax) with |x| <= amax and a finite fp16 scale
+// s = fp16(fp32(amax/7)) of at least 2^-14: the library's encoder is checked on
+// all 16-bit pairs against IEEE arithmetic (tests/test_gpu_exhaustive16.py).
+// On that domain |q| < 7.01, so no clamping is needed.
 __device__ __forceinline__ uint32_t int4x8_corrected(const float2 (&x)[4], float s, float r) {
-  const float2 s2 = make_float2(s, s), r2 = make_float2(r, r);
+  const float2 ns2 = make_float2(-s, -s), r2 = make_float2(r, r);
   const float2 magic = make_float2(kRintMagic, kRintMagic);
   uint32_t b[8];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float2 q1 = __fmul2_rn(x[e], r2);
-    const float2 res = __ffma2_rn(make_float2(-q1.x, -q1.y), s2, x[e]);
+    const float2 res = __ffma2_rn(q1, ns2, x[e]);
     const float2 q = __fadd2_rn(__ffma2_rn(res, r2, q1), magic);
     b[2 * e] = __float_as_uint(q.x);
     b[2 * e + 1] = __float_as_uint(q.y);
@@ -370,20 +389,16 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
     for (int o = 1; o < lanes_per_group; o <<= 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const bool valid = t < si.nv;
-    float s = __fdiv_rn(amax, 7.0f);
-    __half s16 = __float2half_rn(s);
-    if (kScaleF16) s = __half2float(s16);
-    if (!valid) {
-      s = 0.f;
-      s16 = __float2half_rn(0.f);
-    }
+    const float s32 = valid ? div7(amax) : 0.f;  // rows past n_valid: scale 0
+    const __half s16 = __float2half_rn(s32);
+    const float s = kScaleF16 ? __half2float(s16) : s32;
     float2 x[4];
     raw8_to_float2(raw[i], x);
     uint32_t packed;
     if constexpr (kScaleF16 && sizeof(SrcT) == 2) {
-      const float r = __frcp_rn(s);
-      packed = int4x8_corrected(x, s, r);
-      if (!(s >= 0x1p-14f))  // below the verified domain (or s == 0): divide
+      packed = int4x8_corrected(x, s, rcp_approx(s));
+      if (!(s >= 0x1p-14f && s <= 65504.0f))  // outside the verified domain: divide
+        // (s == 0: codes 0; s = +inf, an fp16 scale that overflowed: x / s = 0)
         packed = s != 0.f ? int4x8_divide(x[0], x[1], x[2], x[3], s) : 0u;
     } else {
       packed = int4x8_brackets(x, s, brackets(s, kScaleF16 ? 0x1p-14f : 0x1p-126f), s != 0.f);
