@@ -380,14 +380,18 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
   const int g = (chunk * 8) >> p.group_log2;
   const bool scale_writer = (chunk & (lanes_per_group - 1)) == 0;
   const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
+  uint32_t slow = 0;   // bit i: pass i's scale lies outside the corrected path's domain
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
     const int t = row0 + i * G::kRowsPerPass;
     AbsMax<SrcT> am;
     am.add(raw[i]);
     float amax = am.value();
-    for (int o = 1; o < lanes_per_group; o <<= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // group max over lanes_per_group (4, 8 or 16) neighbouring lanes
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (lanes_per_group > 4) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    if (lanes_per_group > 8) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
     const bool valid = t < si.nv;
     const float s32 = valid ? div7(amax) : 0.f;  // rows past n_valid: scale 0
     const __half s16 = __float2half_rn(s32);
@@ -397,9 +401,12 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
     uint32_t packed;
     if constexpr (kScaleF16 && sizeof(SrcT) == 2) {
       packed = int4x8_corrected(x, s, rcp_approx(s));
-      if (!(s >= 0x1p-14f && s <= 65504.0f))  // outside the verified domain: divide
-        // (s == 0: codes 0; s = +inf, an fp16 scale that overflowed: x / s = 0)
-        packed = s != 0.f ? int4x8_divide(x[0], x[1], x[2], x[3], s) : 0u;
+      // outside the verified domain: s == 0 gives codes 0; other scales (fp16
+      // subnormal, or +inf after an fp16 overflow, where x / s = 0) are
+      // divided in the deferred step below
+      const bool out_of_domain = !(s >= 0x1p-14f && s <= 65504.0f);
+      if (out_of_domain) packed = 0u;
+      slow |= static_cast<uint32_t>(out_of_domain && s != 0.f) << i;
     } else {
       packed = int4x8_brackets(x, s, brackets(s, kScaleF16 ? 0x1p-14f : 0x1p-126f), s != 0.f);
       if (s == 0.f) packed = 0;
@@ -412,6 +419,26 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
       else
         static_cast<float*>(p.scales)[si_] = s;
     }
+  }
+  // Deferred IEEE division for rows whose scale is outside the verified
+  // domain (tiny groups, or amax >= 458752 with fp16 scales); the scale is
+  // read back from where the group's writer lane stored it.
+  __syncwarp();
+  while (slow != 0u) {
+    const int i = __ffs(static_cast<int>(slow)) - 1;
+    slow &= slow - 1u;
+    Raw8<SrcT> r = raw[0];
+#pragma unroll
+    for (int k = 1; k < G::kPasses; ++k)
+      if (i == k) r = raw[k];
+    float2 x[4];
+    raw8_to_float2(r, x);
+    const int t = row0 + i * G::kRowsPerPass;
+    const int64_t si_ = scale_row0 + static_cast<int64_t>(t) * groups_per_row + g;
+    const float sc = kScaleF16 ? __half2float(static_cast<const __half*>(p.scales)[si_])
+                               : static_cast<const float*>(p.scales)[si_];
+    __stcs(reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(t) * (D / 2)),
+           int4x8_divide(x[0], x[1], x[2], x[3], sc));
   }
 }
 
