@@ -11,19 +11,29 @@
 // Work decomposition.  One warp owns a 16-token sub-slab of one (layer,
 // block, kv, head); each lane owns one 8-element chunk of a token row
 // (16 bytes for fp16/bf16, 32 for fp32) per pass, 256/d rows per pass, d/16
-// passes.  CTAs are persistent (two per SM) and step through "units" of 8
-// consecutive sub-slabs.  The pipeline per warp is three deep: the block
-// table entry for unit i+2 is requested, the rows of unit i+1 are loaded
-// (16-bit sources: into a second register buffer), and unit i is quantized
-// and stored - so neither the table lookup nor the row loads sit on the
-// critical path.  The FP8 slab amax needs all B/16 sub-slabs of a block;
+// passes.  A CTA's 8 warps take a "unit" of 8 consecutive sub-slabs.  Two
+// launch shapes, chosen by measurement on GB300: one unit per CTA at 4 CTAs
+// per SM (16-bit INT4, and 16-bit FP8 with blocks over 16 tokens), or
+// persistent CTAs, two per SM, stepping through the units with a three-deep
+// pipeline per warp: the block table entry for unit i+2 is requested, the
+// rows of unit i+1 are loaded (16-bit sources: into a second register
+// buffer), and unit i is quantized and stored - so neither the table lookup
+// nor the row loads sit on the critical path.  The FP8 slab amax needs all
+// B/16 sub-slabs of a block;
 // those warps are in the same CTA and combine through shared memory.  INT4
 // groups lie inside a token row, so INT4 needs no cross-warp step.
 //
 // Quotients without a division per element.  The codes are defined through
 // the IEEE quotient q* = fp32(x / s).
 //
-// FP8 (and INT4 with fp32 sources or fp32 scales): with r = fp32(1/s) and the
+// 16-bit sources (FP8, and INT4 with fp16 scales): the product with a
+// reciprocal of s, corrected once by its exact residual (Markstein), gives
+// q* itself (FP8, correctly rounded reciprocal) or a value with the same
+// rounded integer (INT4, approximate reciprocal).  Both are checked on every
+// 16-bit (x, amax) pair against IEEE arithmetic (fp8x8_corrected,
+// int4x8_corrected); scales outside the checked domain take the division.
+//
+// fp32 sources (and INT4 with fp32 scales): with r = fp32(1/s) and the
 // bracketing multipliers r_lo = fp32(r (1 - 2^-20)), r_hi = fp32(r (1 + 2^-20)),
 // the products q_lo = fp32(x r_lo) and q_hi = fp32(x r_hi) satisfy
 // |q_lo| < |q*| < |q_hi| (three roundings of at most 2^-24 each cannot undo a
@@ -31,16 +41,12 @@
 // are far below the smallest code step and encode alike).  The quantizer is
 // monotone in |q| for a fixed sign, so when q_lo and q_hi give the same code,
 // that is the code of q*.  Where they differ, q* sits at (or within 2^-20 of)
-// a rounding boundary.  With 16-bit sources that is common - a few elements
-// per thousand are exact E4M3 ties, e.g. x = 3/4 amax gives q = 336 - so the
-// main loop only flags the pass, stores the lower-bracket codes, and a
-// deferred step per sub-slab revisits each lane's flagged passes and resolves
-// just the disagreeing elements (an exact FMA-residual test, see
-// fp8_resolve; IEEE division where that test does not apply), re-storing the
-// 8 codes.  A scale below the smallest normal fp32 takes the division path.
-//
-// INT4 with fp16 scales and 16-bit sources: the quotient corrected by its
-// exact residual, checked exhaustively (see int4x8_corrected); no fallback.
+// a rounding boundary: the main loop only flags the pass and stores the
+// lower-bracket codes, and a deferred step per sub-slab revisits each lane's
+// flagged passes and resolves just the disagreeing elements (an exact
+// FMA-residual test, see fp8_resolve; IEEE division where that test does not
+// apply), re-storing the 8 codes.  A scale below the smallest normal fp32
+// takes the division path.
 //
 // Products are formed two at a time (FMUL2 / FFMA2).
 //
@@ -137,17 +143,63 @@ __device__ __forceinline__ uint2 fp8x8(const float2 (&x)[4], float s, const Brac
   return wl;
 }
 
-// Nibble of round_half_even(q) for |q| < 2^22: adding 1.5 * 2^23 leaves the
-// nearest-even integer in the low mantissa bits (one IEEE rounding); its low
-// four bits are the 4-bit two's complement.
-constexpr float kRintMagic = 12582912.0f;
+// 8 E4M3 codes for 16-bit sources: the quotient corrected by its exact
+// residual, q1 = fp32(x r), e = fma(-q1, s, x), q = fma(e, r, q1), with
+// r = fp32(1/s) correctly rounded (Markstein, IBM J. Res. Dev. 34(1), 1990),
+// then one RNE-satfinite conversion.  q equals fp32(x / s) for every pair of
+// fp16 values and every pair of bf16 values (x, amax) with |x| <= amax and
+// s = fp32(amax / 448) >= 2^-90: the library's encoder is checked on all
+// 16-bit pairs against IEEE arithmetic (tests/test_gpu_exhaustive16.py).
+// Exact E4M3 ties (x = 3/4 amax gives q = 336) therefore need no special
+// step.  The corrected quotient of -0 is +0, so the sign bits of the inputs
+// are OR-ed into the codes (for any other input the sign is already there).
+template <typename SrcT>
+__device__ __forceinline__ uint2 fp8x8_corrected(const Raw8<SrcT>& raw, float s, float r) {
+  static_assert(sizeof(SrcT) == 2, "16-bit sources only");
+  float2 x[4];
+  raw8_to_float2(raw, x);
+  const float2 ns2 = make_float2(-s, -s), r2 = make_float2(r, r);
+  uint32_t c[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 q1 = __fmul2_rn(x[e], r2);
+    const float2 res = __ffma2_rn(q1, ns2, x[e]);
+    c[e] = fp8x2(__ffma2_rn(res, r2, q1));
+  }
+  const uint4 v = raw.w[0];  // sign of element k at bit 16k + 15 of the 8 packed inputs
+  return make_uint2((c[0] | (c[1] << 16)) | (__byte_perm(v.x, v.y, 0x7531) & 0x80808080u),
+                    (c[2] | (c[3] << 16)) | (__byte_perm(v.z, v.w, 0x7531) & 0x80808080u));
+}
 
-// Low nibbles of b[0..7] packed, element 2k in the low half of byte k.
+// 8 E4M3 codes by IEEE division (s = 0 gives codes 0).
+template <typename SrcT>
+__device__ __noinline__ uint2 fp8x8_divide(Raw8<SrcT> raw, float s) {
+  if (s == 0.f) return make_uint2(0u, 0u);
+  float2 x[4];
+  raw8_to_float2(raw, x);
+  uint32_t c[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) c[e] = fp8x2(make_float2(__fdiv_rn(x[e].x, s), __fdiv_rn(x[e].y, s)));
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// round_half_even(q) + 8 for |q| <= 7.5: adding 1.5 * 2^23 + 8 (an even
+// integer, in the binade where the fp32 spacing is 1) rounds q to the
+// nearest-even integer in one IEEE rounding and leaves rint(q) + 8, in
+// [1, 15], as the whole low byte of the sum's bit pattern (the bits above it
+// are those of 1.5 * 2^23).
+constexpr float kRintMagic = 12582920.0f;
+
+// The 4-bit two's complement codes from eight biased bytes b[e] = code_e + 8
+// (in the low byte of each word), element 2k in the low half of byte k:
+// byte k = (b[2k] + 16 b[2k+1]) ^ 0x88 - the two biased nibbles cannot carry
+// into each other, and flipping bit 3 of code + 8 gives the code's nibble.
 __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&b)[8]) {
   uint32_t p[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) p[k] = (b[2 * k] & 0xfu) | ((b[2 * k + 1] << 4) & 0xf0u);
-  return __byte_perm(__byte_perm(p[0], p[1], 0x0040), __byte_perm(p[2], p[3], 0x0040), 0x5410);
+  for (int k = 0; k < 4; ++k) p[k] = b[2 * k] + (b[2 * k + 1] << 4);
+  return __byte_perm(__byte_perm(p[0], p[1], 0x0040), __byte_perm(p[2], p[3], 0x0040), 0x5410) ^
+         0x88888888u;
 }
 
 // fp32(a / 7) for every non-negative finite fp32 a, without a division: the
@@ -265,20 +317,28 @@ __device__ __forceinline__ int slot_errors(const EncodeParams& p, const SlotInfo
   return bad;
 }
 
-template <typename SrcT, int D>
+// The rows of a warp's sub-slab.  kZeroPad: rows past n_valid (and every row
+// of an inactive warp or a bad slot) read as zeros.  Otherwise every row is
+// loaded: a bad slot or an inactive warp reads slot 0, and rows past n_valid
+// lie inside the slot, so all loads stay in bounds; the caller discards them.
+template <typename SrcT, int D, bool kZeroPad>
 __device__ __forceinline__ void load_rows(const EncodeParams& p, const Where& w, const SlotInfo& si,
                                           int chunk, int rr, Raw8<SrcT> (&raw)[EncodeGeom<D>::kPasses]) {
   using G = EncodeGeom<D>;
   const bool ok = w.active && slot_errors(p, si) == 0;
+  const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
+  const int64_t row_stride = static_cast<int64_t>(p.H) * D;
   const SrcT* base = static_cast<const SrcT*>(w.kv ? p.v : p.k) +
                      static_cast<int64_t>(w.l) * p.layer_stride +
-                     static_cast<int64_t>(ok ? si.slot : 0) * p.slot_stride + w.h * D + chunk * 8;
-  const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
+                     static_cast<int64_t>(ok ? si.slot : 0) * p.slot_stride + w.h * D + chunk * 8 +
+                     row0 * row_stride;
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
-    const int t = row0 + i * G::kRowsPerPass;
-    raw[i] = (ok && t < si.nv) ? load8_stream(base + static_cast<int64_t>(t) * p.H * D)
-                               : raw8_zero<SrcT>();
+    const SrcT* src = base + i * G::kRowsPerPass * row_stride;
+    if constexpr (kZeroPad)
+      raw[i] = (ok && row0 + i * G::kRowsPerPass < si.nv) ? load8_stream(src) : raw8_zero<SrcT>();
+    else
+      raw[i] = load8_stream(src);
   }
 }
 
@@ -308,9 +368,27 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
   if (!ok) return;
 
   const float s = __fdiv_rn(amax, 448.0f);
-  const Brackets br = brackets(s, 0x1p-126f);
   uint8_t* out = p.codes + w.slab * static_cast<int64_t>(p.B) * D + chunk * 8;
   const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
+  if constexpr (sizeof(SrcT) == 2) {
+    // Rows past n_valid hold zeros, whose codes are 0.  The branch is uniform
+    // over the warp (one slab); scales below 2^-90 (bf16 slabs with amax below
+    // about 2^-81) and s = 0 take the IEEE division.
+    uint2* dst = reinterpret_cast<uint2*>(out + static_cast<int64_t>(row0) * D);
+    constexpr int kPassStride = G::kRowsPerPass * D / 8;  // in uint2
+    if (s >= 0x1p-90f) {
+      const float r = __frcp_rn(s);
+#pragma unroll
+      for (int i = 0; i < G::kPasses; ++i) __stcs(dst + i * kPassStride, fp8x8_corrected(raw[i], s, r));
+    } else {
+#pragma unroll
+      for (int i = 0; i < G::kPasses; ++i) __stcs(dst + i * kPassStride, fp8x8_divide(raw[i], s));
+    }
+    if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
+    return;
+  }
+  // fp32 sources: the bracketed products with the deferred exact tie step.
+  const Brackets br = brackets(s, 0x1p-126f);
   uint32_t pend = 0;  // bit i: in pass i the brackets disagree somewhere in this lane's chunk
 #pragma unroll
   for (int i = 0; i < G::kPasses; ++i) {
@@ -362,7 +440,10 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
   if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
 }
 
-template <typename SrcT, int D, bool kScaleF16>
+// kGroupLog2: log2 of the group size when fixed at compile time, else 0.
+// Rows past n_valid are loaded but never used: their scale is 0 and their
+// codes are 0.
+template <typename SrcT, int D, bool kScaleF16, int kGroupLog2>
 __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where& w,
                                               const SlotInfo& si, int chunk, int rr, int lane,
                                               const Raw8<SrcT> (&raw)[EncodeGeom<D>::kPasses]) {
@@ -373,11 +454,12 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
     if (lane == 0) flag_error(p.err, bad);
     return;
   }
-  const int lanes_per_group = 1 << (p.group_log2 - 3);  // 4, 8 or 16; groups never straddle rows
-  const int groups_per_row = D >> p.group_log2;
+  const int group_log2 = kGroupLog2 ? kGroupLog2 : p.group_log2;
+  const int lanes_per_group = 1 << (group_log2 - 3);  // 4, 8 or 16; groups never straddle rows
+  const int groups_per_row = D >> group_log2;
   uint8_t* out = p.codes + w.slab * static_cast<int64_t>(p.B) * (D / 2) + chunk * 4;
   const int64_t scale_row0 = w.slab * static_cast<int64_t>(p.B) * groups_per_row;
-  const int g = (chunk * 8) >> p.group_log2;
+  const int g = (chunk * 8) >> group_log2;
   const bool scale_writer = (chunk & (lanes_per_group - 1)) == 0;
   const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
   uint32_t slow = 0;   // bit i: pass i's scale lies outside the corrected path's domain
@@ -448,7 +530,8 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
 // the persistent pipeline is faster for FP8 with 16-token blocks, the flat
 // launch for FP8 with larger blocks (whose units meet at a CTA barrier) and
 // for INT4.
-template <typename SrcT, int D, int kWire, bool kFlat>
+// kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
+template <typename SrcT, int D, int kWire, bool kFlat, int kGroupLog2>
 __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams p) {
   using G = EncodeGeom<D>;
   constexpr bool kDoubleBuffer = !kFlat && sizeof(SrcT) == 2;
@@ -464,22 +547,27 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
     if constexpr (kWire == 0)
       quantize_fp8<SrcT, D>(p, w, si, chunk, rr, warp, lane, s_amax[parity], raw);
     else
-      quantize_int4<SrcT, D, kWire == 1>(p, w, si, chunk, rr, lane, raw);
+      quantize_int4<SrcT, D, kWire == 1, kGroupLog2>(p, w, si, chunk, rr, lane, raw);
   };
+  constexpr bool kZeroPad = kWire == 0;
 
   Where w0 = locate(p.grid, c * kWarps + warp);
   SlotInfo s0 = fetch_slot(p, w0);
-  if constexpr (kDoubleBuffer) {
+  if constexpr (kFlat) {  // the grid has one CTA per unit
+    Raw8<SrcT> cur[G::kPasses];
+    load_rows<SrcT, D, kZeroPad>(p, w0, s0, chunk, rr, cur);
+    process(w0, s0, cur, 0);
+  } else if constexpr (kDoubleBuffer) {
     Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
     SlotInfo s1 = fetch_slot(p, w1);
     Raw8<SrcT> cur[G::kPasses];
-    load_rows<SrcT, D>(p, w0, s0, chunk, rr, cur);
+    load_rows<SrcT, D, kZeroPad>(p, w0, s0, chunk, rr, cur);
     int parity = 0;
     for (; c < p.grid.units; c += stride) {
       const Where w2 = locate(p.grid, (c + 2 * stride) * kWarps + warp);
       const SlotInfo s2 = fetch_slot(p, w2);
       Raw8<SrcT> nxt[G::kPasses];
-      load_rows<SrcT, D>(p, w1, s1, chunk, rr, nxt);
+      load_rows<SrcT, D, kZeroPad>(p, w1, s1, chunk, rr, nxt);
       process(w0, s0, cur, parity);
       parity ^= 1;
       w0 = w1;
@@ -495,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
       const Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
       const SlotInfo s1 = fetch_slot(p, w1);
       Raw8<SrcT> cur[G::kPasses];
-      load_rows<SrcT, D>(p, w0, s0, chunk, rr, cur);
+      load_rows<SrcT, D, kZeroPad>(p, w0, s0, chunk, rr, cur);
       process(w0, s0, cur, parity);
       parity ^= 1;
       w0 = w1;
@@ -504,21 +592,35 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
   }
 }
 
-template <typename SrcT, int D, int kWire>
-cudaError_t encode_t(const EncodeParams& p, cudaStream_t s) {
-  // fp32 sources hold twice the registers per row: always the persistent shape.
-  bool launched = false;
-  if constexpr (sizeof(SrcT) == 2) {
-    if (kWire != 0 || p.B > kRowsPerWarp) {
-      k_encode<SrcT, D, kWire, true><<<p.grid.units, kThreads, 0, s>>>(p);
-      launched = true;
+// Launch shape: 16-bit INT4, and 16-bit FP8 with blocks over 16 tokens, one
+// unit per CTA; everything else persistent (fp32 sources hold twice the
+// registers per row).
+template <typename SrcT, int D, int kWire, int kGroupLog2>
+void encode_launch(const EncodeParams& p, cudaStream_t s) {
+  if constexpr (sizeof(SrcT) == 2 && kWire != 0) {
+    k_encode<SrcT, D, kWire, true, kGroupLog2><<<p.grid.units, kThreads, 0, s>>>(p);
+  } else {
+    if constexpr (sizeof(SrcT) == 2) {
+      if (p.B > kRowsPerWarp) {
+        k_encode<SrcT, D, kWire, true, kGroupLog2><<<p.grid.units, kThreads, 0, s>>>(p);
+        return;
+      }
     }
-  }
-  if (!launched) {
     const uint32_t grid = static_cast<uint32_t>(
         std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * 2));
-    k_encode<SrcT, D, kWire, false><<<grid, kThreads, 0, s>>>(p);
+    k_encode<SrcT, D, kWire, false, kGroupLog2><<<grid, kThreads, 0, s>>>(p);
   }
+}
+
+template <typename SrcT, int D, int kWire>
+cudaError_t encode_t(const EncodeParams& p, cudaStream_t s) {
+  if constexpr (kWire != 0) {
+    if (p.group_log2 == 5) {
+      encode_launch<SrcT, D, kWire, 5>(p, s);
+      return cudaGetLastError();
+    }
+  }
+  encode_launch<SrcT, D, kWire, 0>(p, s);
   return cudaGetLastError();
 }
 

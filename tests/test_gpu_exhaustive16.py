@@ -15,9 +15,10 @@ Every division is tensor by tensor: torch turns a division by a Python
 scalar into a multiplication by its reciprocal, which is not the IEEE
 quotient (it misses fp16 ties such as amax / 7 = 6.5 * 2^-24).
 
-This covers the kernels' division-free quotient paths (bracketed products with
-the exact tie resolver for FP8; the residual-corrected quotient for INT4) on
-their whole 16-bit input domain.
+This covers the kernels' division-free quotient paths for 16-bit sources (the
+residual-corrected quotient, for FP8 and for INT4) and the IEEE-division
+paths they hand tiny or overflowing scales to, on the whole 16-bit input
+domain.
 """
 import pytest
 import torch
