@@ -524,6 +524,96 @@ __device__ __forceinline__ void quantize_int4(const EncodeParams& p, const Where
   }
 }
 
+// INT4 with fp16 scales from 16-bit sources, 16 channels per lane: half the
+// group reductions, scale computations, and code and scale stores per
+// element of the 8-channel layout.  A lane loads 32 contiguous bytes of a
+// token row (two 16-byte loads), d/16 lanes cover a row, 512/d rows per pass.
+// One unit of 8 sub-slabs per CTA; warps are independent.
+#ifndef HC_ENCODE_WIDE_MIN_BLOCKS
+#define HC_ENCODE_WIDE_MIN_BLOCKS 4
+#endif
+template <typename SrcT, int D, int kGroupLog2>
+__global__ void __launch_bounds__(kThreads, HC_ENCODE_WIDE_MIN_BLOCKS) k_encode_int4_wide(EncodeParams p) {
+  static_assert(sizeof(SrcT) == 2, "16-bit sources only");
+  constexpr int kLanesPerRow = D / 16;
+  constexpr int kRowsPerPass = 32 / kLanesPerRow;
+  constexpr int kPasses = kRowsPerWarp / kRowsPerPass;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = lane % kLanesPerRow, rr = lane / kLanesPerRow;
+  const Where w = locate(p.grid, blockIdx.x * kWarps + warp);
+  if (!w.active) return;
+  const SlotInfo si = fetch_slot(p, w);
+  const int bad = slot_errors(p, si);
+  if (bad) {
+    if (lane == 0) flag_error(p.err, bad);
+    return;
+  }
+  const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + rr;
+  const int64_t row_stride = static_cast<int64_t>(p.H) * D;
+  const SrcT* src = static_cast<const SrcT*>(w.kv ? p.v : p.k) +
+                    static_cast<int64_t>(w.l) * p.layer_stride +
+                    static_cast<int64_t>(si.slot) * p.slot_stride + w.h * D + chunk * 16 +
+                    row0 * row_stride;
+  // Every row of the slot is loaded; rows past n_valid get scale 0 and codes 0.
+  Raw8<SrcT> raw[kPasses][2];
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    raw[i][0] = load8_stream(src + i * kRowsPerPass * row_stride);
+    raw[i][1] = load8_stream(src + i * kRowsPerPass * row_stride + 8);
+  }
+  const int group_log2 = kGroupLog2 ? kGroupLog2 : p.group_log2;
+  const int lanes_per_group = 1 << (group_log2 - 4);  // 2, 4 or 8
+  const int groups_per_row = D >> group_log2;
+  const int g = (chunk * 16) >> group_log2;
+  const bool scale_writer = (chunk & (lanes_per_group - 1)) == 0;
+  uint2* out = reinterpret_cast<uint2*>(p.codes + w.slab * static_cast<int64_t>(p.B) * (D / 2) +
+                                        static_cast<int64_t>(row0) * (D / 2) + chunk * 8);
+  __half* sc = static_cast<__half*>(p.scales) + w.slab * static_cast<int64_t>(p.B) * groups_per_row +
+               static_cast<int64_t>(row0) * groups_per_row + g;
+  uint32_t slow = 0;  // bit i: pass i's scale lies outside the corrected path's domain
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    AbsMax<SrcT> am;
+    am.add(raw[i][0]);
+    am.add(raw[i][1]);
+    float amax = am.value();
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    if (lanes_per_group > 2) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (lanes_per_group > 4) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const bool valid = row0 + i * kRowsPerPass < si.nv;
+    const __half s16 = __float2half_rn(valid ? div7(amax) : 0.f);
+    const float s = __half2float(s16);
+    const float r = rcp_approx(s);
+    float2 x0[4], x1[4];
+    raw8_to_float2(raw[i][0], x0);
+    raw8_to_float2(raw[i][1], x1);
+    uint2 packed = make_uint2(int4x8_corrected(x0, s, r), int4x8_corrected(x1, s, r));
+    // outside the verified domain: s == 0 gives codes 0; other scales are
+    // divided in the deferred step below
+    const bool out_of_domain = !(s >= 0x1p-14f && s <= 65504.0f);
+    if (out_of_domain) packed = make_uint2(0u, 0u);
+    slow |= static_cast<uint32_t>(out_of_domain && s != 0.f) << i;
+    __stcs(out + i * kRowsPerPass * (D / 16), packed);
+    if (scale_writer) sc[i * kRowsPerPass * groups_per_row] = s16;
+  }
+  // Deferred IEEE division (rows whose scale is outside the verified domain);
+  // the rows are read again rather than kept in registers.
+  __syncwarp();
+  while (slow != 0u) {
+    const int i = __ffs(static_cast<int>(slow)) - 1;
+    slow &= slow - 1u;
+    const Raw8<SrcT> r0 = load8_stream(src + i * kRowsPerPass * row_stride);
+    const Raw8<SrcT> r1 = load8_stream(src + i * kRowsPerPass * row_stride + 8);
+    float2 x0[4], x1[4];
+    raw8_to_float2(r0, x0);
+    raw8_to_float2(r1, x1);
+    const float s = __half2float(sc[i * kRowsPerPass * groups_per_row]);
+    __stcs(out + i * kRowsPerPass * (D / 16),
+           make_uint2(int4x8_divide(x0[0], x0[1], x0[2], x0[3], s),
+                      int4x8_divide(x1[0], x1[1], x1[2], x1[3], s)));
+  }
+}
+
 // kWire: 0 = FP8, 1 = INT4 fp16 scales, 2 = INT4 fp32 scales.
 // kFlat: one unit per CTA at 4 CTAs per SM; otherwise persistent CTAs (2 per
 // SM) with the per-warp double buffer for 16-bit sources.  Measured on GB300,
@@ -597,7 +687,9 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
 // registers per row).
 template <typename SrcT, int D, int kWire, int kGroupLog2>
 void encode_launch(const EncodeParams& p, cudaStream_t s) {
-  if constexpr (sizeof(SrcT) == 2 && kWire != 0) {
+  if constexpr (sizeof(SrcT) == 2 && kWire == 1) {
+    k_encode_int4_wide<SrcT, D, kGroupLog2><<<p.grid.units, kThreads, 0, s>>>(p);
+  } else if constexpr (sizeof(SrcT) == 2 && kWire != 0) {
     k_encode<SrcT, D, kWire, true, kGroupLog2><<<p.grid.units, kThreads, 0, s>>>(p);
   } else {
     if constexpr (sizeof(SrcT) == 2) {

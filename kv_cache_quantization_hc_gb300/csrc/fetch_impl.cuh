@@ -122,19 +122,88 @@ __device__ __forceinline__ void int4x8_to_float2(uint32_t c, float s, float2 (&x
   }
 }
 
+// The same for scales that are fp16 values (at most 11 significant bits),
+// one fma per two elements: each biased code b = code + 8 in [1, 15] is put
+// in mantissa bits 19..22 of 1.0, giving m = 1 + b/16 exactly, and
+// x = fma(m, 16 s, -24 s) = (b - 8) s.  16 s and 24 s = 3 * 8 s are exact in
+// fp32 (13 significant bits at most), and so is the result code * s (15 at
+// most), so the fma's one rounding changes nothing.
+__device__ __forceinline__ void int4x8_to_float2_f16s(uint32_t c, float s, float2 (&x)[4]) {
+  // byte i of even / odd: 0x80 | (b << 3) for the low / high nibble of byte i
+  // of c (the 0x80 is the low exponent bit of 1.0; xor 0x40 applies the bias)
+  const uint32_t even = ((c << 3) & 0x78787878u) ^ 0xC0C0C0C0u;
+  const uint32_t odd = ((c >> 1) & 0x78787878u) ^ 0xC0C0C0C0u;
+  const float2 s16 = make_float2(16.0f * s, 16.0f * s);
+  const float2 c24 = make_float2(-24.0f * s, -24.0f * s);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // bytes [0, 0, byte i, 0x3F]: the fp32 pattern of 1 + b/16
+    const float2 m = make_float2(__uint_as_float(__byte_perm(even, 0x3F000000u, 0x7044 + 0x100 * i)),
+                                 __uint_as_float(__byte_perm(odd, 0x3F000000u, 0x7044 + 0x100 * i)));
+    x[i] = __ffma2_rn(m, s16, c24);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void raw8_to_f2(const Raw8<T>& r, float2 (&x)[4]) {
   raw8_to_float2(r, x);
 }
 
-template <int W, typename OutT, int D, bool kHalfSplit, bool kScaleF16>
-__device__ __forceinline__ void load_stage(const FetchParams& p, const Where& w, const Info& in,
-                                           int q, int r, Stage<W, OutT, D>& st) {
+// The wire rows of a sub-slab are loaded whatever the block table says: their
+// addresses come from the sub-slab index alone (an inactive warp reads slab
+// 0), padding rows exist on the wire, and rows that are not stored are
+// discarded - so the loads need not wait for the table entries.  The rotation
+// table row is read only for a valid block.
+template <int W, typename OutT, int D, bool kHalfSplit, bool kScaleF16, int kGroupLog2>
+__device__ __forceinline__ void load_codes(const FetchParams& p, const Where& w, int q, int r,
+                                           Stage<W, OutT, D>& st) {
   using G = FetchGeom<D>;
-  const bool ok = w.active && info_errors(p, in) == 0;
   const int row0 = static_cast<int>(w.sub) * kRowsPerWarp + r;
-  const int64_t slab_rows = w.slab * static_cast<int64_t>(p.B);
+  const int64_t rows = w.slab * static_cast<int64_t>(p.B) + row0;
   const int c_lo = 8 * q, c_hi = D / 2 + 8 * q;
+  if (W == kFp8) st.s_slab = __ldg(static_cast<const float*>(p.scales) + w.slab);
+  if constexpr (W == kFp8) {
+    const uint8_t* b = static_cast<const uint8_t*>(p.codes) + rows * D;
+#pragma unroll
+    for (int i = 0; i < G::kPasses; ++i) {
+      st.cd[i].lo = __ldcs(reinterpret_cast<const uint2*>(b + i * G::kRowsPerPass * D + c_lo));
+      st.cd[i].hi = __ldcs(reinterpret_cast<const uint2*>(b + i * G::kRowsPerPass * D + c_hi));
+    }
+  } else if constexpr (W == kInt4) {
+    const uint8_t* b = static_cast<const uint8_t*>(p.codes) + rows * (D / 2);
+    const int group_log2 = kGroupLog2 ? kGroupLog2 : p.group_log2;
+    const int gpr = D >> group_log2;  // groups per row
+    const int64_t sb = rows * gpr;
+    const int g_lo = c_lo >> group_log2, g_hi = c_hi >> group_log2;
+#pragma unroll
+    for (int i = 0; i < G::kPasses; ++i) {
+      st.cd[i].lo = __ldcs(reinterpret_cast<const unsigned int*>(b + i * G::kRowsPerPass * (D / 2) + c_lo / 2));
+      st.cd[i].hi = __ldcs(reinterpret_cast<const unsigned int*>(b + i * G::kRowsPerPass * (D / 2) + c_hi / 2));
+      const int64_t si = sb + i * G::kRowsPerPass * gpr;
+      if (kScaleF16) {
+        const __half* S = static_cast<const __half*>(p.scales);
+        st.cd[i].s_lo = __half2float(__ldg(S + si + g_lo));
+        st.cd[i].s_hi = __half2float(__ldg(S + si + g_hi));
+      } else {
+        const float* S = static_cast<const float*>(p.scales);
+        st.cd[i].s_lo = __ldg(S + si + g_lo);
+        st.cd[i].s_hi = __ldg(S + si + g_hi);
+      }
+    }
+  } else {
+    const OutT* b = static_cast<const OutT*>(p.codes) + rows * D;
+#pragma unroll
+    for (int i = 0; i < G::kPasses; ++i) {
+      st.cd[i].lo = load8_stream(b + i * G::kRowsPerPass * D + c_lo);
+      st.cd[i].hi = load8_stream(b + i * G::kRowsPerPass * D + c_hi);
+    }
+  }
+}
+
+template <int W, typename OutT, int D, bool kHalfSplit>
+__device__ __forceinline__ void load_table(const FetchParams& p, const Where& w, const Info& in,
+                                           int q, Stage<W, OutT, D>& st) {
+  const bool ok = w.active && info_errors(p, in) == 0;
   if (ok && w.kv == 0) {
     const float4* tab = reinterpret_cast<const float4*>(p.table + static_cast<int64_t>(in.di) * D);
     // float4 k of a table row holds pairs 2k and 2k+1 as (c, s, c, s)
@@ -152,37 +221,6 @@ __device__ __forceinline__ void load_stage(const FetchParams& p, const Where& w,
     for (int i = 0; i < 4; ++i) {
       st.cs[i] = make_float2(t4[i].x, t4[i].z);
       st.sn[i] = make_float2(t4[i].y, t4[i].w);
-    }
-  }
-  if (W == kFp8) st.s_slab = ok ? __ldg(static_cast<const float*>(p.scales) + w.slab) : 0.f;
-#pragma unroll
-  for (int i = 0; i < G::kPasses; ++i) {
-    const int t = row0 + i * G::kRowsPerPass;
-    const bool valid = ok && t < in.nv;
-    const int64_t row = slab_rows + t;
-    if constexpr (W == kFp8) {
-      const uint8_t* b = static_cast<const uint8_t*>(p.codes) + row * D;
-      st.cd[i].lo = valid ? __ldcs(reinterpret_cast<const uint2*>(b + c_lo)) : make_uint2(0, 0);
-      st.cd[i].hi = valid ? __ldcs(reinterpret_cast<const uint2*>(b + c_hi)) : make_uint2(0, 0);
-    } else if constexpr (W == kInt4) {
-      const uint8_t* b = static_cast<const uint8_t*>(p.codes) + row * (D / 2);
-      st.cd[i].lo = valid ? __ldcs(reinterpret_cast<const unsigned int*>(b + c_lo / 2)) : 0u;
-      st.cd[i].hi = valid ? __ldcs(reinterpret_cast<const unsigned int*>(b + c_hi / 2)) : 0u;
-      const int64_t sb = row * (D >> p.group_log2);
-      const int g_lo = c_lo >> p.group_log2, g_hi = c_hi >> p.group_log2;
-      if (kScaleF16) {
-        const __half* S = static_cast<const __half*>(p.scales);
-        st.cd[i].s_lo = valid ? __half2float(__ldg(S + sb + g_lo)) : 0.f;
-        st.cd[i].s_hi = valid ? __half2float(__ldg(S + sb + g_hi)) : 0.f;
-      } else {
-        const float* S = static_cast<const float*>(p.scales);
-        st.cd[i].s_lo = valid ? __ldg(S + sb + g_lo) : 0.f;
-        st.cd[i].s_hi = valid ? __ldg(S + sb + g_hi) : 0.f;
-      }
-    } else {
-      const OutT* b = static_cast<const OutT*>(p.codes) + row * D;
-      st.cd[i].lo = valid ? load8_stream(b + c_lo) : raw8_zero<OutT>();
-      st.cd[i].hi = valid ? load8_stream(b + c_hi) : raw8_zero<OutT>();
     }
   }
 }
@@ -245,8 +283,13 @@ __device__ __forceinline__ void process_stage(const FetchParams& p, const Where&
       fp8x8_to_float2(st.cd[i].lo, st.s_slab, lo);
       fp8x8_to_float2(st.cd[i].hi, st.s_slab, hi);
     } else if constexpr (W == kInt4) {
-      int4x8_to_float2(st.cd[i].lo, st.cd[i].s_lo, lo);
-      int4x8_to_float2(st.cd[i].hi, st.cd[i].s_hi, hi);
+      if constexpr (kScaleF16) {
+        int4x8_to_float2_f16s(st.cd[i].lo, st.cd[i].s_lo, lo);
+        int4x8_to_float2_f16s(st.cd[i].hi, st.cd[i].s_hi, hi);
+      } else {
+        int4x8_to_float2(st.cd[i].lo, st.cd[i].s_lo, lo);
+        int4x8_to_float2(st.cd[i].hi, st.cd[i].s_hi, hi);
+      }
     } else {
       raw8_to_f2(st.cd[i].lo, lo);
       raw8_to_f2(st.cd[i].hi, hi);
@@ -279,7 +322,8 @@ __device__ __forceinline__ void process_stage(const FetchParams& p, const Where&
   }
 }
 
-template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16>
+// kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
+template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16, int kGroupLog2>
 __global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchParams p) {
   using St = Stage<W, OutT, D>;
   constexpr bool kDoubleBuffer = HC_FETCH_DOUBLE_BUFFER && W != kRaw;
@@ -294,12 +338,14 @@ __global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchPa
     Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
     Info i1 = fetch_info(p, w1);
     St cur;
-    load_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, cur);
+    load_codes<W, OutT, D, kHalfSplit, kScaleF16, kGroupLog2>(p, w0, q, r, cur);
+    load_table<W, OutT, D, kHalfSplit>(p, w0, i0, q, cur);
     for (; c < p.grid.units; c += stride) {
       const Where w2 = locate(p.grid, (c + 2 * stride) * kWarps + warp);
       const Info i2 = fetch_info(p, w2);
       St nxt;
-      load_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w1, i1, q, r, nxt);
+      load_codes<W, OutT, D, kHalfSplit, kScaleF16, kGroupLog2>(p, w1, q, r, nxt);
+      load_table<W, OutT, D, kHalfSplit>(p, w1, i1, q, nxt);
       process_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, lane, cur);
       w0 = w1;
       i0 = i1;
@@ -308,14 +354,15 @@ __global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchPa
       cur = nxt;
     }
   } else {
-    for (; c < p.grid.units; c += stride) {
-      const Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
-      const Info i1 = fetch_info(p, w1);
+    for (;;) {
       St cur;
-      load_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, cur);
+      load_codes<W, OutT, D, kHalfSplit, kScaleF16, kGroupLog2>(p, w0, q, r, cur);
+      load_table<W, OutT, D, kHalfSplit>(p, w0, i0, q, cur);
       process_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, lane, cur);
-      w0 = w1;
-      i0 = i1;
+      c += stride;
+      if (c >= p.grid.units) break;  // one unit per CTA: no next unit
+      w0 = locate(p.grid, c * kWarps + warp);
+      i0 = fetch_info(p, w0);
     }
   }
 }
@@ -324,7 +371,10 @@ template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16>
 cudaError_t launch_t(const FetchParams& p, cudaStream_t s) {
   const uint32_t grid = static_cast<uint32_t>(
       std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * HC_FETCH_CTAS_PER_SM));
-  k_fetch<OutT, D, W, kHalfSplit, kScaleF16><<<grid, kThreads, 0, s>>>(p);
+  if (W == kInt4 && p.group_log2 == 5)
+    k_fetch<OutT, D, W, kHalfSplit, kScaleF16, W == kInt4 ? 5 : 0><<<grid, kThreads, 0, s>>>(p);
+  else
+    k_fetch<OutT, D, W, kHalfSplit, kScaleF16, 0><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
