@@ -21,6 +21,10 @@ The pages give no memory layout; the readings implemented here:
 * wire: [L, NB, 2, H, B, d] (kv = 0 is K, 1 is V) of E4M3 bytes with one fp32
   scale per (layer, block, kv, head); INT4 packs [L, NB, 2, H, B, d/2] bytes
   with one scale per (layer, block, kv, head, token, group of g channels);
+* the row-scaled FP8 wire ("pages layout"): the same E4M3 bytes with one
+  scale per (layer, block, kv, head, token) row of d channels, fp16 by
+  default - the granularity whose sizes reproduce the printed FP8 frame
+  (133,120 payload bytes for 131,072 fp16 values, 1.97x);
 * n_valid[j] tokens of block j are real; the rest are padding: excluded from
   amax, encoded as 0 (INT4 scale 0), never written by fetch;
 * one delta-m per block (a block moves as a unit).
@@ -79,6 +83,30 @@ def encode_int4(paged_k, paged_v, src_slots, n_valid=None, group=32, scale_dtype
     ints, scales = quant.int4_quantize(g, valid, scale_dtype)
     ints = ints.reshape(L, NB, 2, H, B, d)
     return quant.int4_pack(ints), scales
+
+
+def encode_fp8_rows(paged_k, paged_v, src_slots, n_valid=None, scale_dtype="f16"):
+    """FP8 E4M3 encode, one scale per (layer, block, kv, head, token) row of d.
+
+    s = fp32(amax / 448), rounded to fp16 when scale_dtype is "f16"; the codes
+    use the stored scale (a scale that overflows fp16 is +inf and gives codes
+    of x / inf = +-0).  Padding rows get scale 0 and codes 0.
+
+    Returns codes uint8 [L, NB, 2, H, B, d] and scales float64 [L, NB, 2, H, B].
+    """
+    slabs = gather_slabs(paged_k, paged_v, src_slots)
+    L, NB, _, H, B, d = slabs.shape
+    valid = _valid_rows(n_valid, NB, B)[None, :, None, None, :, None]
+    valid = np.broadcast_to(valid, slabs.shape)
+    with np.errstate(over="ignore"):
+        return quant.fp8_quantize(slabs, valid, scale_dtype)
+
+
+def decode_fp8_rows(codes, scales):
+    """[L, NB, 2, H, B, d] exact dequantized values (code * stored row scale;
+    a row whose fp16 scale overflowed to +inf decodes to 0 * inf = NaN)."""
+    with np.errstate(invalid="ignore"):
+        return quant.fp8_dequantize(codes, scales)
 
 
 def decode_fp8(codes, scales):

@@ -141,3 +141,51 @@ def test_kv_bytes_pins(golden):
     llama = kvbytes.kv_bytes(80, 8, 128, 65536, 1)
     assert llama == 10737418240
     assert round(llama / 2 ** 30) == golden["llama3_70b_64k_fp8_gb_approx"]
+
+
+# --- row-scaled FP8 (the pages' frame layout) ------------------------------------
+def test_encode_fp8_rows_reproduces_the_printed_frame_payload(golden):
+    """One 64-token block of 8 heads x 128 channels, K and V, is 131,072 fp16
+    values: with one fp16 scale per (token, head) row its FP8 payload is the
+    133,120 bytes under the printed 133,188-byte frame (1.97x)."""
+    rng = np.random.default_rng(7)
+    L, S, B, H, d = 1, 2, 64, 8, 128
+    pk = round_to(rng.standard_normal((L, S, B, H, d)), "f16")
+    pv = round_to(rng.standard_normal((L, S, B, H, d)), "f16")
+    codes, scales = paged.encode_fp8_rows(pk, pv, [1])
+    assert codes.shape == (1, 1, 2, H, B, d) and scales.shape == (1, 1, 2, H, B)
+    payload = codes.size + scales.size * 2
+    assert payload == 133120 and 0 < golden["fp8_tcp_frame_bytes"] - payload < 128
+    assert round(2 * pk[0, 1].size * 2 / payload, 2) == golden["fp8_compression_ratio"]
+    # same codes as the group quantizer applied to each gathered row
+    rows = np.stack([pk[0, 1], pv[0, 1]]).transpose(0, 2, 1, 3)       # [2, H, B, d]
+    c2, s2 = quant.fp8_quantize(rows, scale_dtype="f16")
+    assert np.array_equal(codes[0, 0], c2) and np.array_equal(scales[0, 0], s2)
+
+
+def test_encode_fp8_rows_rules():
+    rng = np.random.default_rng(8)
+    L, S, B, H, d = 2, 4, 16, 2, 64
+    pk = round_to(rng.standard_normal((L, S, B, H, d)) * 3, "bf16")
+    pv = round_to(rng.standard_normal((L, S, B, H, d)), "bf16")
+    pk[1, 2, 3, 1, :] = 0.0
+    pk[1, 2, 3, 1, 5] = -0.0
+    pk[0, 3, 0, 0, 7] = 3.0e38                      # fp16 scale overflows to +inf
+    codes, s = paged.encode_fp8_rows(pk, pv, [2, 3], n_valid=[16, 9])
+    assert np.all(s[:, 1, :, :, 9:] == 0) and np.all(codes[:, 1, :, :, 9:] == 0)   # padding rows
+    assert s[1, 0, 0, 1, 3] == 0 and np.all(codes[1, 0, 0, 1, 3] == 0)             # zero row (-0 -> 0)
+    assert np.isinf(s[0, 1, 0, 0, 0])
+    row = pk[0, 3, 0, 0]
+    assert np.array_equal(codes[0, 1, 0, 0, 0], np.where(np.signbit(row), 0x80, 0).astype(np.uint8))
+    # elsewhere: the amax element codes to +-448, scales are fp16(fp32(amax/448))
+    sl = pk[0, 2, :, 1, :]
+    want = round_to(round_to(np.abs(sl).max(-1) / 448.0, "f32"), "f16")
+    assert np.array_equal(s[0, 0, 0, 1], want)
+    i = np.argmax(np.abs(sl), axis=-1)
+    assert np.all((codes[0, 0, 0, 1][np.arange(B), i] & 0x7F) == 0x7E)
+    dec = paged.decode_fp8_rows(codes, s)
+    ok = np.isfinite(s)[..., None] & (s[..., None] > 0)
+    err = np.abs(dec - paged.gather_slabs(pk, pv, [2, 3]))
+    valid = np.ones_like(err, bool)
+    valid[:, 1, :, :, 9:] = False
+    assert np.all(err[ok & valid] <= (np.abs(paged.gather_slabs(pk, pv, [2, 3])) * 2.0 ** -4 + 2.0 ** -9 * np.broadcast_to(s[..., None], err.shape))[ok & valid])
