@@ -34,8 +34,14 @@ if ROOT not in sys.path:
 METRIC = "KV fetch+rotate+scatter GB/s and tokens/s; % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {
-    "k_encode": ["encode.cu", "hc_internal.cuh", "fastdiv.h"],
+    "k_encode": ["encode.cu", "encode_common.cuh", "hc_internal.cuh", "fastdiv.h"],
     "k_fetch": ["fetch_impl.cuh", "fetch_fp8.cu", "hc_internal.cuh", "fastdiv.h"],
+    "k_encode_fp8_rows": ["encode_rows.cu", "encode_common.cuh", "hc_internal.cuh", "fastdiv.h"],
+    "k_fetch_fp8_rows": ["fetch_impl.cuh", "fetch_fp8_rows.cu", "hc_internal.cuh", "fastdiv.h"],
+}
+CODECS = {
+    "fp8": "FP8 E4M3 wire (per-block-head fp32 scale)",
+    "fp8_rows": "FP8 E4M3 wire (per-token-head fp16 scale, the pages' frame layout)",
 }
 
 
@@ -157,14 +163,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ workload
-def algorithmic_bytes(w, blk):
+def algorithmic_bytes(w, blk, codec="fp8"):
     """Bytes the method must move, per kernel, for one call over all layers."""
     L, H, d, T, NB = w.L, w.H, w.d, blk.tokens(), blk.nb
     src_b = {"f32": 4, "f16": 2, "bf16": 2}[w.src_dtype]
     out_b = {"f32": 4, "f16": 2, "bf16": 2}[w.out_dtype]
     kv_elems = 2 * L * T * H * d
     codes = kv_elems
-    scales = L * NB * 2 * H * 4
+    scales = L * NB * 2 * H * 4 if codec == "fp8" else 2 * L * T * H * 2
     n_distinct = len(np.unique(blk.delta_m))
     table = n_distinct * (d // 2) * 8
     encode = kv_elems * src_b + codes + scales + NB * 4
@@ -172,7 +178,7 @@ def algorithmic_bytes(w, blk):
     return {"encode": encode, "table": table + n_distinct * 4, "fetch": fetch}
 
 
-def setup_device(w, blk, device):
+def setup_device(w, blk, device, codec="fp8"):
     import torch
     from kv_cache_quantization_hc_gb300 import path as kvpath
     import workloads
@@ -181,7 +187,7 @@ def setup_device(w, blk, device):
     shape = (w.L, blk.num_dst_slots, blk.B, w.H, w.d)
     dst_k = torch.empty(shape, dtype=torch.bfloat16, device=device)
     dst_v = torch.empty(shape, dtype=torch.bfloat16, device=device)
-    p = kvpath.from_blocks(w, blk, "fp8", device=device)
+    p = kvpath.from_blocks(w, blk, codec, device=device, scale_dtype="f16")
     return p, src_k, src_v, dst_k, dst_v
 
 
@@ -203,8 +209,8 @@ def run_ours(args):
     if args.layers:
         w.L = args.layers
     blk = w.blocks[0]
-    p, src_k, src_v, dst_k, dst_v = setup_device(w, blk, device)
-    nbytes = algorithmic_bytes(w, blk)
+    p, src_k, src_v, dst_k, dst_v = setup_device(w, blk, device, args.codec)
+    nbytes = algorithmic_bytes(w, blk, args.codec)
     step_bytes = sum(nbytes.values())
     stream = torch.cuda.current_stream(device)
 
@@ -253,9 +259,12 @@ def run_ours(args):
                    "bytes_per_launch": nbytes[k], "gbs": nbytes[k] / avg / 1e9}
     dominant = max(("encode", "fetch"), key=lambda k: kern[k]["avg_ms"])
     kname = {"encode": "k_encode", "fetch": "k_fetch"}[dominant]
+    if args.codec == "fp8_rows":
+        kname += "_fp8_rows"
     traffic = profiled_traffic(kname, "qwen3_8b") if not args.layers else None
     achieved = kern[dominant]["gbs"]
 
+    crc = run_crc(args, p, device) if args.crc else None
     e2e = None
     if "e2e" in args.legs:
         e2e = run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device)
@@ -270,11 +279,13 @@ def run_ours(args):
             "ms_per_step": max_s / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"qwen3_8b: {w.L} layers x {w.H} KV heads x d{w.d}, "
-                                   f"{blk.tokens()} tokens, block {blk.B}, fp16 paged -> FP8 E4M3 "
-                                   f"wire (per-block-head fp32 scale) -> bf16 paged, delta-m +4096, "
+                                   f"{blk.tokens()} tokens, block {blk.B}, fp16 paged -> "
+                                   f"{CODECS[args.codec]} -> bf16 paged, delta-m +4096, "
                                    f"half-split RoPE base 1e6, shuffled block tables",
                        "layers": w.L, "tokens": blk.tokens(), "block_size": blk.B,
-                       "storage": {"source": w.src_dtype, "wire": "e4m3", "destination": w.out_dtype},
+                       "storage": {"source": w.src_dtype, "wire": "e4m3",
+                                   "scales": "f32 per block-head" if args.codec == "fp8" else "f16 per token-head",
+                                   "destination": w.out_dtype},
                        "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (working set %.1f GB per step)" % (step_bytes / 1e9),
                        "parallelism": f"replicas x{world}"},
@@ -291,10 +302,35 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if crc is not None:
+            line["crc32"] = crc
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_crc(args, p, device):
+    """CRC-32 of the step's wire (one unit per (layer, block): its codes, then
+    its scales), timed alone with CUDA events after the step's own timing."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    out = torch.empty(p.L * p.nb, dtype=torch.int32, device=device)
+    nbytes = p.codes.numel() * p.codes.element_size() + p.scales.numel() * p.scales.element_size()
+    for _ in range(3):
+        p.crc32(out, stream)
+    reps = max(3, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        a.record(stream)
+        p.crc32(out, stream)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    avg = statistics.mean(a.elapsed_time(b) / 1e3 for a, b in evs)
+    peak, _ = measured_peaks()
+    return {"kernel": "k_crc32", "units": p.L * p.nb, "bytes_per_launch": nbytes, "launches": reps,
+            "avg_ms": avg * 1e3, "gbs": nbytes / avg / 1e9, "frac": nbytes / avg / 1e9 / peak,
+            "bound": "hbm (read only)"}
 
 
 def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device):
@@ -317,7 +353,7 @@ def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device):
     h_dst_v = torch.empty(dst_v.shape, dtype=dst_v.dtype, pin_memory=True)
     w1 = copy.copy(w)
     w1.L = 1
-    p1 = kvpath.from_blocks(w1, blk, "fp8", device=device)
+    p1 = kvpath.from_blocks(w1, blk, args.codec, device=device, scale_dtype="f16")
     ls = LayerStream(p1, src_k.shape[1:], src_k.dtype, dst_k.shape[1:], dst_k.dtype, device)
     tables = [p1.src_slots, p1.dst_slots, p1.delta_m, p1.delta_idx]
     h_tables = [t.cpu().pin_memory() for t in tables]
@@ -558,6 +594,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-blocks", type=int, default=16)
     ap.add_argument("--wire", choices=["int4", "fp8"], default="int4", help="ragged workload's wire format")
+    ap.add_argument("--codec", choices=sorted(CODECS), default="fp8",
+                    help="wire of the qwen3_8b step: per-block-head FP8 (default) or per-row FP8")
+    ap.add_argument("--crc", action="store_true",
+                    help="also time the CRC-32 of the step's wire (reported as crc32)")
     args = ap.parse_args(argv)
     args.legs = set(args.legs.split(","))
     args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps

@@ -36,13 +36,16 @@
  * Wire buffers, for a call over n_blocks blocks (kv = 0 is K, 1 is V):
  *   FP8 : codes  u8  [n_layers][n_blocks][2][n_kv_heads][block_size][d_head]
  *         scales f32 [n_layers][n_blocks][2][n_kv_heads]           (per block, head)
+ *   FP8_ROWS: codes as FP8
+ *         scales f16|f32 [n_layers][n_blocks][2][n_kv_heads][block_size] (per token row)
  *   INT4: codes  u8  [n_layers][n_blocks][2][n_kv_heads][block_size][d_head/2]
  *                    (channel 2k in the low nibble, 2k+1 in the high nibble,
  *                     4-bit two's complement, values -7..7)
  *         scales f16|f32 [n_layers][n_blocks][2][n_kv_heads][block_size][d_head/group]
  *   RAW : values in the paged dtype, [n_layers][n_blocks][2][n_kv_heads][block_size][d_head]
  *         (unquantized; no scales).
- * Padding rows (token t >= n_valid[j]) are encoded as code 0 (INT4 scale 0).
+ * Padding rows (token t >= n_valid[j]) are encoded as code 0 (INT4 and
+ * FP8_ROWS scale 0).
  */
 #ifndef HC_H_
 #define HC_H_
@@ -53,7 +56,7 @@
 extern "C" {
 #endif
 
-#define HC_API_VERSION 1
+#define HC_API_VERSION 2
 
 typedef enum hc_status {
   HC_OK = 0,
@@ -67,7 +70,12 @@ typedef enum hc_dtype { HC_F32 = 0, HC_F16 = 1, HC_BF16 = 2 } hc_dtype;
 /* Which channels form a rotation pair: (2i, 2i+1), or (i, i + d_head/2). */
 typedef enum hc_pairing { HC_PAIR_INTERLEAVED = 0, HC_PAIR_HALF_SPLIT = 1 } hc_pairing;
 
-typedef enum hc_wire { HC_WIRE_FP8 = 0, HC_WIRE_INT4 = 1, HC_WIRE_RAW = 2 } hc_wire;
+typedef enum hc_wire {
+  HC_WIRE_FP8 = 0,     /* E4M3, one fp32 scale per (layer, block, kv, head) */
+  HC_WIRE_INT4 = 1,    /* grouped INT4 */
+  HC_WIRE_RAW = 2,     /* unquantized */
+  HC_WIRE_FP8_ROWS = 3 /* E4M3, one scale per (layer, block, kv, head, token) row */
+} hc_wire;
 
 /* Bits ORed into *err_flag by the device. */
 #define HC_DEVERR_SLOT 1   /* src_slots[j] or dst_slots[j] outside [0, num_slots) */
@@ -133,6 +141,28 @@ int hc_encode_int4(const void* paged_k, const void* paged_v, const hc_paged_desc
                    int32_t group, int32_t scale_dtype, uint8_t* codes, void* scales,
                    int32_t* err_flag, void* stream);
 
+/* hc_encode_fp8_rows: as hc_encode_fp8, but one scale per (layer, block, kv,
+ * head, token) row of d_head channels - the granularity whose sizes match the
+ * FP8 frame the page prints (131,072 fp16 values -> 131,072 code bytes +
+ * 1,024 fp16 scales = 133,120 bytes, 1.97x):
+ *   amax = max |x| over the row,  s32 = fp32(amax / 448),
+ *   s = fp16_rne(s32) if scale_dtype == HC_F16, else s32,
+ *   code = E4M3(fp32(x / s)) with the stored s, nearest even, saturating at
+ *   +-448, sign kept.  A row with s == 0 gets all-zero codes; an fp16 scale
+ *   that overflows (amax above about 2.9e7) is stored as +inf and gives the
+ *   codes of x / inf = +-0.  Padding rows get scale 0 and codes 0.
+ * [HyperCache page, "Example output" part B, "FP8 (E4M3) Wire Quantization"
+ *  and "Live TCP Socket Fetch" frame size.]
+ *
+ *   scale_dtype : HC_F16 or HC_F32
+ *   codes       : device u8, FP8_ROWS code layout above, 16-byte aligned
+ *   scales      : device f16 or f32, FP8_ROWS scale layout above, aligned to its element
+ * Other arguments as for hc_encode_fp8. */
+int hc_encode_fp8_rows(const void* paged_k, const void* paged_v, const hc_paged_desc* desc,
+                       const int32_t* src_slots, const int32_t* n_valid, int32_t n_blocks,
+                       int32_t scale_dtype, uint8_t* codes, void* scales, int32_t* err_flag,
+                       void* stream);
+
 /* hc_build_delta_sincos: the rotation table of the fetch.  For each distinct
  * delta-m value n and pair i < d_head/2:
  *   theta_i = inv_freq[i] if inv_freq != NULL, else rope_base^(-2i/d_head);
@@ -161,11 +191,11 @@ int hc_build_delta_sincos(const int32_t* delta_m, int32_t n_distinct, int32_t d_
  * [HyperCache page, "Core Design" relative RoPE paragraph; "Example output"
  *  part B, "Live TCP Socket Fetch + On-The-Fly RoPE".]
  *
- *   wire        : hc_wire (FP8, INT4 or RAW)
+ *   wire        : hc_wire (FP8, INT4, RAW or FP8_ROWS)
  *   codes       : device, wire layout above (RAW: paged dtype), 16-byte aligned
  *   scales      : device, wire scale layout above (RAW: ignored, may be NULL)
  *   group       : INT4 group size (32, 64, 128, <= d_head); ignored otherwise
- *   scale_dtype : INT4: HC_F16 or HC_F32; ignored otherwise
+ *   scale_dtype : INT4 and FP8_ROWS: HC_F16 or HC_F32; ignored otherwise
  *   table       : device f32 [n_distinct][d_head/2][2] from hc_build_delta_sincos,
  *                 16-byte aligned
  *   delta_idx   : device int32 [n_blocks], row of `table` for block j
@@ -184,6 +214,24 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
                             const int32_t* n_valid, int32_t n_blocks, void* paged_k,
                             void* paged_v, const hc_paged_desc* desc, int32_t* err_flag,
                             void* stream);
+
+/* hc_crc32: CRC-32 of encoded units, for tamper detection of stored or sent
+ * blocks.  Unit u < n_units is the byte string
+ *   a[u*a_stride .. u*a_stride + a_bytes) followed by b[u*b_stride .. u*b_stride + b_bytes)
+ * (for instance one (layer, block)'s codes followed by its scales), and
+ * crc[u] is its CRC-32/ISO-HDLC, the CRC of zlib and PNG: polynomial
+ * 0x04C11DB7 processed bit-reflected, initial register 0xFFFFFFFF, final
+ * xor 0xFFFFFFFF (check value 0xCBF43926 for the ASCII "123456789").
+ * [HyperCache page, "Example output" part B, "INT4 (Grouped) L3 Disk
+ *  (.hckv + CRC32)", and the CRC32 tamper-detection tests it lists.]
+ *
+ *   a        : device, 16-byte aligned; a_stride a multiple of 16; a_bytes >= 0
+ *   b        : device, any alignment, or NULL when b_bytes == 0
+ *   n_units  : >= 0; 0 launches nothing
+ *   crc      : device u32 [n_units], written in full
+ * Returns HC_OK, HC_ERR_INVALID_ARG or HC_ERR_CUDA. */
+int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, int64_t b_bytes,
+             int64_t b_stride, int32_t n_units, uint32_t* crc, void* stream);
 
 /* Human-readable name of an hc_status value (static string, never NULL). */
 const char* hc_status_string(int32_t status);

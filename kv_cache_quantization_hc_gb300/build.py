@@ -19,8 +19,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhc.so")
 
-SOURCES = ["api.cu", "encode.cu", "fetch_fp8.cu", "fetch_int4.cu", "fetch_raw.cu", "table.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("hc_internal.cuh", "fetch_impl.cuh")] + [
+SOURCES = ["api.cu", "encode.cu", "encode_rows.cu", "fetch_fp8.cu", "fetch_fp8_rows.cu",
+           "fetch_int4.cu", "fetch_raw.cu", "table.cu", "crc32.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("hc_internal.cuh", "fetch_impl.cuh", "encode_common.cuh",
+                                            "fastdiv.h")] + [
     os.path.join(INCLUDE, "hc.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]

@@ -122,6 +122,26 @@ int hc_encode_int4(const void* paged_k, const void* paged_v, const hc_paged_desc
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int hc_encode_fp8_rows(const void* paged_k, const void* paged_v, const hc_paged_desc* desc,
+                       const int32_t* src_slots, const int32_t* n_valid, int32_t n_blocks,
+                       int32_t scale_dtype, uint8_t* codes, void* scales, int32_t* err_flag,
+                       void* stream) {
+  int st = check_paged(desc, paged_k, paged_v);
+  if (st != HC_OK) return st;
+  if (n_blocks < 0) return HC_ERR_INVALID_ARG;
+  if (!src_slots || !codes || !scales || !err_flag) return HC_ERR_INVALID_ARG;
+  if (scale_dtype != HC_F16 && scale_dtype != HC_F32) return HC_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(scales, scale_dtype == HC_F16 ? 2 : 4) ||
+      !aligned(err_flag, 4) || !aligned(src_slots, 4) || (n_valid && !aligned(n_valid, 4)))
+    return HC_ERR_INVALID_ARG;
+  if (!grid_fits(desc, n_blocks)) return HC_ERR_INVALID_ARG;
+  if (n_blocks == 0) return HC_OK;
+  const hc::EncodeParams p = encode_params(paged_k, paged_v, desc, src_slots, n_valid, n_blocks,
+                                           codes, scales, err_flag, 0);
+  return record(hc::launch_encode_fp8_rows(desc->dtype, desc->d_head, scale_dtype == HC_F16, p,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int hc_build_delta_sincos(const int32_t* delta_m, int32_t n_distinct, int32_t d_head,
                           double rope_base, const double* inv_freq, float* table,
                           void* stream) {
@@ -155,7 +175,8 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
   int st = check_paged(desc, paged_k, paged_v);
   if (st != HC_OK) return st;
   if (n_blocks < 0) return HC_ERR_INVALID_ARG;
-  if (wire != HC_WIRE_FP8 && wire != HC_WIRE_INT4 && wire != HC_WIRE_RAW)
+  if (wire != HC_WIRE_FP8 && wire != HC_WIRE_INT4 && wire != HC_WIRE_RAW &&
+      wire != HC_WIRE_FP8_ROWS)
     return HC_ERR_INVALID_ARG;
   if (pairing != HC_PAIR_INTERLEAVED && pairing != HC_PAIR_HALF_SPLIT) return HC_ERR_INVALID_ARG;
   if (!codes || !table || !delta_idx || !dst_slots || !err_flag) return HC_ERR_INVALID_ARG;
@@ -168,6 +189,10 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
     if (!aligned(scales, scale_dtype == HC_F16 ? 2 : 4)) return HC_ERR_INVALID_ARG;
   }
   if (wire == HC_WIRE_FP8 && !aligned(scales, 4)) return HC_ERR_INVALID_ARG;
+  if (wire == HC_WIRE_FP8_ROWS) {
+    if (scale_dtype != HC_F16 && scale_dtype != HC_F32) return HC_ERR_INVALID_ARG;
+    if (!aligned(scales, scale_dtype == HC_F16 ? 2 : 4)) return HC_ERR_INVALID_ARG;
+  }
   if (!aligned(codes, 16) || !aligned(table, 16) || !aligned(delta_idx, 4) ||
       !aligned(dst_slots, 4) || !aligned(err_flag, 4) || (n_valid && !aligned(n_valid, 4)))
     return HC_ERR_INVALID_ARG;
@@ -202,8 +227,33 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
     case HC_WIRE_INT4:
       return record(
           hc::launch_fetch_int4(desc->dtype, desc->d_head, half, scale_dtype == HC_F16, p, s));
+    case HC_WIRE_FP8_ROWS:
+      return record(hc::launch_fetch_fp8_rows(desc->dtype, desc->d_head, half,
+                                              scale_dtype == HC_F16, p, s));
     default: return record(hc::launch_fetch_raw(desc->dtype, desc->d_head, half, p, s));
   }
+}
+
+int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, int64_t b_bytes,
+             int64_t b_stride, int32_t n_units, uint32_t* crc, void* stream) {
+  if (n_units < 0 || a_bytes < 0 || b_bytes < 0 || a_stride < 0 || b_stride < 0)
+    return HC_ERR_INVALID_ARG;
+  if (!crc || (a_bytes > 0 && !a) || (b_bytes > 0 && !b)) return HC_ERR_INVALID_ARG;
+  if ((a && !aligned(a, 16)) || a_stride % 16 || !aligned(crc, 4)) return HC_ERR_INVALID_ARG;
+  if (n_units > 1 && (a_stride < a_bytes || (b_bytes > 0 && b_stride < b_bytes)))
+    return HC_ERR_INVALID_ARG;
+  if (n_units == 0) return HC_OK;
+  hc::CrcParams p;
+  std::memset(&p, 0, sizeof p);
+  p.a = static_cast<const uint8_t*>(a);
+  p.b = static_cast<const uint8_t*>(b);
+  p.a_bytes = a_bytes;
+  p.a_stride = a_stride;
+  p.b_bytes = b_bytes;
+  p.b_stride = b_stride;
+  p.n_units = static_cast<uint32_t>(n_units);
+  p.crc = crc;
+  return record(hc::launch_crc32(p, static_cast<cudaStream_t>(stream)));
 }
 
 const char* hc_status_string(int32_t status) {

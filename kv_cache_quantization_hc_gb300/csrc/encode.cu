@@ -54,7 +54,7 @@
 // written with streaming stores.
 #include <algorithm>
 
-#include "hc_internal.cuh"
+#include "encode_common.cuh"
 
 namespace hc {
 namespace {
@@ -80,10 +80,6 @@ __device__ __forceinline__ Brackets brackets(float s, float min_scale) {
   b.hi = make_float2(hi, hi);
   b.ok = s >= min_scale;
   return b;
-}
-
-__device__ __forceinline__ uint32_t fp8x2(float2 v) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
 __device__ __forceinline__ uint32_t fp8x1(float v) { return fp8x2(make_float2(v, 0.f)) & 0xffu; }
@@ -143,46 +139,6 @@ __device__ __forceinline__ uint2 fp8x8(const float2 (&x)[4], float s, const Brac
   return wl;
 }
 
-// 8 E4M3 codes for 16-bit sources: the quotient corrected by its exact
-// residual, q1 = fp32(x r), e = fma(-q1, s, x), q = fma(e, r, q1), with
-// r = fp32(1/s) correctly rounded (Markstein, IBM J. Res. Dev. 34(1), 1990),
-// then one RNE-satfinite conversion.  q equals fp32(x / s) for every pair of
-// fp16 values and every pair of bf16 values (x, amax) with |x| <= amax and
-// s = fp32(amax / 448) >= 2^-90: the library's encoder is checked on all
-// 16-bit pairs against IEEE arithmetic (tests/test_gpu_exhaustive16.py).
-// Exact E4M3 ties (x = 3/4 amax gives q = 336) therefore need no special
-// step.  The corrected quotient of -0 is +0, so the sign bits of the inputs
-// are OR-ed into the codes (for any other input the sign is already there).
-template <typename SrcT>
-__device__ __forceinline__ uint2 fp8x8_corrected(const Raw8<SrcT>& raw, float s, float r) {
-  static_assert(sizeof(SrcT) == 2, "16-bit sources only");
-  float2 x[4];
-  raw8_to_float2(raw, x);
-  const float2 ns2 = make_float2(-s, -s), r2 = make_float2(r, r);
-  uint32_t c[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 q1 = __fmul2_rn(x[e], r2);
-    const float2 res = __ffma2_rn(q1, ns2, x[e]);
-    c[e] = fp8x2(__ffma2_rn(res, r2, q1));
-  }
-  const uint4 v = raw.w[0];  // sign of element k at bit 16k + 15 of the 8 packed inputs
-  return make_uint2((c[0] | (c[1] << 16)) | (__byte_perm(v.x, v.y, 0x7531) & 0x80808080u),
-                    (c[2] | (c[3] << 16)) | (__byte_perm(v.z, v.w, 0x7531) & 0x80808080u));
-}
-
-// 8 E4M3 codes by IEEE division (s = 0 gives codes 0).
-template <typename SrcT>
-__device__ __noinline__ uint2 fp8x8_divide(Raw8<SrcT> raw, float s) {
-  if (s == 0.f) return make_uint2(0u, 0u);
-  float2 x[4];
-  raw8_to_float2(raw, x);
-  uint32_t c[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) c[e] = fp8x2(make_float2(__fdiv_rn(x[e].x, s), __fdiv_rn(x[e].y, s)));
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
 // round_half_even(q) + 8 for |q| <= 7.5: adding 1.5 * 2^23 + 8 (an even
 // integer, in the binade where the fp32 spacing is 1) rounds q to the
 // nearest-even integer in one IEEE rounding and leaves rint(q) + 8, in
@@ -200,16 +156,6 @@ __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&b)[8]) {
   for (int k = 0; k < 4; ++k) p[k] = b[2 * k] + (b[2 * k + 1] << 4);
   return __byte_perm(__byte_perm(p[0], p[1], 0x0040), __byte_perm(p[2], p[3], 0x0040), 0x5410) ^
          0x88888888u;
-}
-
-// fp32(a / 7) for every non-negative finite fp32 a, without a division: the
-// product with fp32(1/7) is corrected by its exact residual (Markstein's
-// correction, as in int4x8_corrected).  Checked against the IEEE division on
-// the GPU for all 2^31 non-negative finite fp32 values: no mismatch.
-__device__ __forceinline__ float div7(float a) {
-  const float r7 = 0.142857149f;  // fp32(1/7)
-  const float q1 = a * r7;
-  return fmaf(fmaf(-q1, 7.0f, a), r7, q1);
 }
 
 // The hardware reciprocal approximation (at most 1 ulp of error).
@@ -294,27 +240,6 @@ __device__ __forceinline__ uint32_t int4x8_brackets(const float2 (&x)[4], float 
   for (int e = 0; e < 8; ++e) need |= static_cast<uint32_t>(valid && (slow || bl[e] != bh[e])) << e;
   if (__any_sync(0xffffffffu, need != 0u)) out = int4x8_fix(x[0], x[1], x[2], x[3], s, out, need);
   return out;
-}
-
-// Block-table entries a warp needs for one unit.
-struct SlotInfo {
-  int32_t slot, nv;
-};
-
-__device__ __forceinline__ SlotInfo fetch_slot(const EncodeParams& p, const Where& w) {
-  SlotInfo s{0, 0};
-  if (w.active) {
-    s.slot = __ldg(p.src_slots + w.j);
-    s.nv = p.n_valid ? __ldg(p.n_valid + w.j) : p.B;
-  }
-  return s;
-}
-
-__device__ __forceinline__ int slot_errors(const EncodeParams& p, const SlotInfo& s) {
-  int bad = 0;
-  if (s.slot < 0 || s.slot >= p.num_slots) bad |= HC_DEVERR_SLOT;
-  if (s.nv < 1 || s.nv > p.B) bad |= HC_DEVERR_NVALID;
-  return bad;
 }
 
 // The rows of a warp's sub-slab.  kZeroPad: rows past n_valid (and every row

@@ -34,7 +34,7 @@
 namespace hc {
 namespace fetch_detail {
 
-enum WireKind { kFp8 = 0, kInt4 = 1, kRaw = 2 };
+enum WireKind { kFp8 = 0, kInt4 = 1, kRaw = 2, kFp8Rows = 3 };
 
 template <int D>
 struct FetchGeom {
@@ -58,6 +58,11 @@ struct Codes<kInt4, OutT> {
 template <typename OutT>
 struct Codes<kRaw, OutT> {
   Raw8<OutT> lo, hi;
+};
+template <typename OutT>
+struct Codes<kFp8Rows, OutT> {
+  uint2 lo, hi;  // 8 E4M3 codes each
+  float s;       // the row's scale
 };
 
 // Everything one warp holds for one sub-slab before decoding it.
@@ -162,12 +167,17 @@ __device__ __forceinline__ void load_codes(const FetchParams& p, const Where& w,
   const int64_t rows = w.slab * static_cast<int64_t>(p.B) + row0;
   const int c_lo = 8 * q, c_hi = D / 2 + 8 * q;
   if (W == kFp8) st.s_slab = __ldg(static_cast<const float*>(p.scales) + w.slab);
-  if constexpr (W == kFp8) {
+  if constexpr (W == kFp8 || W == kFp8Rows) {
     const uint8_t* b = static_cast<const uint8_t*>(p.codes) + rows * D;
 #pragma unroll
     for (int i = 0; i < G::kPasses; ++i) {
       st.cd[i].lo = __ldcs(reinterpret_cast<const uint2*>(b + i * G::kRowsPerPass * D + c_lo));
       st.cd[i].hi = __ldcs(reinterpret_cast<const uint2*>(b + i * G::kRowsPerPass * D + c_hi));
+      if constexpr (W == kFp8Rows) {
+        const int64_t si = rows + i * G::kRowsPerPass;
+        st.cd[i].s = kScaleF16 ? __half2float(__ldg(static_cast<const __half*>(p.scales) + si))
+                               : __ldg(static_cast<const float*>(p.scales) + si);
+      }
     }
   } else if constexpr (W == kInt4) {
     const uint8_t* b = static_cast<const uint8_t*>(p.codes) + rows * (D / 2);
@@ -282,6 +292,9 @@ __device__ __forceinline__ void process_stage(const FetchParams& p, const Where&
     if constexpr (W == kFp8) {
       fp8x8_to_float2(st.cd[i].lo, st.s_slab, lo);
       fp8x8_to_float2(st.cd[i].hi, st.s_slab, hi);
+    } else if constexpr (W == kFp8Rows) {
+      fp8x8_to_float2(st.cd[i].lo, st.cd[i].s, lo);
+      fp8x8_to_float2(st.cd[i].hi, st.cd[i].s, hi);
     } else if constexpr (W == kInt4) {
       if constexpr (kScaleF16) {
         int4x8_to_float2_f16s(st.cd[i].lo, st.cd[i].s_lo, lo);

@@ -86,8 +86,30 @@ struct TableParams {
   double theta[128];
 };
 
+// CRC-32 of units a[u*a_stride ..+a_bytes) ++ b[u*b_stride ..+b_bytes), one
+// warp per unit.  Lane k < 31 takes bytes [k*chunk, (k+1)*chunk) of the a
+// part, lane 31 the rest of it and the b part; each lane's register is moved
+// to the end of the unit by multiplying with lane_shift[k] = x^(8 * bytes
+// after its part) mod P, and init_term adds the initial register's
+// contribution and the final xor.  Constants are built on the host.
+struct CrcParams {
+  const uint8_t* a;
+  const uint8_t* b;
+  int64_t a_bytes, a_stride, b_bytes, b_stride;
+  int64_t chunk;  // a multiple of 128
+  uint32_t n_units;
+  uint32_t* crc;
+  uint32_t lane_shift[32];
+  uint32_t init_term;
+};
+
 // Launchers: return the launch's cudaError_t.  `dtype`/`out_dtype` are hc_dtype.
 cudaError_t launch_encode_fp8(int dtype, int d, const EncodeParams& p, cudaStream_t s);
+cudaError_t launch_encode_fp8_rows(int dtype, int d, bool scale_f16, const EncodeParams& p,
+                                   cudaStream_t s);
+cudaError_t launch_fetch_fp8_rows(int out_dtype, int d, bool half_split, bool scale_f16,
+                                  const FetchParams& p, cudaStream_t s);
+cudaError_t launch_crc32(const CrcParams& p, cudaStream_t s);
 cudaError_t launch_encode_int4(int dtype, int d, bool scale_f16, const EncodeParams& p,
                                cudaStream_t s);
 cudaError_t launch_fetch_fp8(int out_dtype, int d, bool half_split, const FetchParams& p,

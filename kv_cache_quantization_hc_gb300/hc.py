@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_PKG, "libhc.so")
 HC_OK, HC_ERR_INVALID_ARG, HC_ERR_UNSUPPORTED, HC_ERR_CUDA = 0, -1, -2, -3
 HC_F32, HC_F16, HC_BF16 = 0, 1, 2
 HC_PAIR_INTERLEAVED, HC_PAIR_HALF_SPLIT = 0, 1
-HC_WIRE_FP8, HC_WIRE_INT4, HC_WIRE_RAW = 0, 1, 2
+HC_WIRE_FP8, HC_WIRE_INT4, HC_WIRE_RAW, HC_WIRE_FP8_ROWS = 0, 1, 2, 3
 HC_DEVERR_SLOT, HC_DEVERR_DELTA, HC_DEVERR_NVALID = 1, 2, 4
 
 DTYPE_NAMES = {"f32": HC_F32, "f16": HC_F16, "bf16": HC_BF16}
@@ -51,11 +51,14 @@ def lib():
         desc_p = ctypes.POINTER(hc_paged_desc)
         L.hc_encode_fp8.argtypes = [_P, _P, desc_p, _P, _P, _I32, _P, _P, _P, _P]
         L.hc_encode_int4.argtypes = [_P, _P, desc_p, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]
+        L.hc_encode_fp8_rows.argtypes = [_P, _P, desc_p, _P, _P, _I32, _I32, _P, _P, _P, _P]
         L.hc_build_delta_sincos.argtypes = [_P, _I32, _I32, ctypes.c_double, _P, _P, _P]
         L.hc_fetch_rotate_scatter.argtypes = [_I32, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _P, _P,
                                               _I32, _P, _P, desc_p, _P, _P]
-        for fn in ("hc_encode_fp8", "hc_encode_int4", "hc_build_delta_sincos",
-                   "hc_fetch_rotate_scatter"):
+        _I64 = ctypes.c_int64
+        L.hc_crc32.argtypes = [_P, _I64, _I64, _P, _I64, _I64, _I32, _P, _P]
+        for fn in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
+                   "hc_fetch_rotate_scatter", "hc_crc32"):
             getattr(L, fn).restype = ctypes.c_int
         L.hc_status_string.argtypes = [_I32]
         L.hc_status_string.restype = ctypes.c_char_p
@@ -132,6 +135,19 @@ def hc_encode_int4(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, group, 
         n_blocks, group, scale_dtype, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
 
 
+def hc_encode_fp8_rows(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, scale_dtype, codes,
+                       scales, err_flag, stream=None):
+    _check("hc_encode_fp8_rows", lib().hc_encode_fp8_rows(
+        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
+        n_blocks, scale_dtype, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
+
+
+def hc_crc32(a, a_bytes, a_stride, b, b_bytes, b_stride, n_units, crc, stream=None):
+    _check("hc_crc32", lib().hc_crc32(
+        _ptr(a), a_bytes, a_stride, _ptr(b), b_bytes, b_stride, n_units, _ptr(crc),
+        _stream(stream)))
+
+
 def hc_build_delta_sincos(delta_m, n_distinct, d_head, rope_base, inv_freq, table, stream=None):
     _check("hc_build_delta_sincos", lib().hc_build_delta_sincos(
         _ptr(delta_m), n_distinct, d_head, float(rope_base), _ptr(inv_freq), _ptr(table),
@@ -157,4 +173,6 @@ def wire_shapes(n_layers, n_blocks, H, B, d, wire, group=32):
         return (n_layers, n_blocks, 2, H, B, d // 2), "u8", (n_layers, n_blocks, 2, H, B, d // group)
     if wire == HC_WIRE_RAW:
         return (n_layers, n_blocks, 2, H, B, d), "paged", None
+    if wire == HC_WIRE_FP8_ROWS:
+        return (n_layers, n_blocks, 2, H, B, d), "u8", (n_layers, n_blocks, 2, H, B)
     raise ValueError(wire)

@@ -15,7 +15,8 @@ import torch
 
 from . import hc
 
-WIRES = {"fp8": hc.HC_WIRE_FP8, "int4": hc.HC_WIRE_INT4, "raw": hc.HC_WIRE_RAW}
+WIRES = {"fp8": hc.HC_WIRE_FP8, "int4": hc.HC_WIRE_INT4, "raw": hc.HC_WIRE_RAW,
+         "fp8_rows": hc.HC_WIRE_FP8_ROWS}
 _TORCH = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -64,6 +65,9 @@ class KVPath:
         elif self.wire == hc.HC_WIRE_INT4:
             hc.hc_encode_int4(src_k, src_v, desc, self.src_slots, self.n_valid, self.nb,
                               self.group, self.scale_dtype, codes, scales, self.err, stream)
+        elif self.wire == hc.HC_WIRE_FP8_ROWS:
+            hc.hc_encode_fp8_rows(src_k, src_v, desc, self.src_slots, self.n_valid, self.nb,
+                                  self.scale_dtype, codes, scales, self.err, stream)
         else:
             raise ValueError("the RAW wire has no encode step")
 
@@ -79,6 +83,20 @@ class KVPath:
                                    self.table, self.delta_idx, self.n_distinct, self.pairing,
                                    self.dst_slots, self.n_valid, self.nb, dst_k, dst_v, desc,
                                    self.err, stream)
+
+    def crc32(self, out=None, stream=None):
+        """CRC-32 of every (layer, block)'s wire bytes: its codes for K and V,
+        then its scales (device uint32 [n_layers * n_blocks], layer-major)."""
+        L, nb = self.L, self.nb
+        out = torch.empty(L * nb, dtype=torch.int32, device=self.codes.device) if out is None else out
+        a_bytes = self.codes[0, 0].numel() * self.codes.element_size()
+        if self.scales is None:
+            hc.hc_crc32(self.codes, a_bytes, a_bytes, None, 0, 0, L * nb, out, stream)
+        else:
+            b_bytes = self.scales[0, 0].numel() * self.scales.element_size()
+            hc.hc_crc32(self.codes, a_bytes, a_bytes, self.scales, b_bytes, b_bytes, L * nb, out,
+                        stream)
+        return out
 
     def error_bits(self):
         return int(self.err.item())

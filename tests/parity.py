@@ -9,8 +9,9 @@ the C ABI, to the CUDA path, and compares:
 * fetched K: fp32 output within 2e-6 x the row's max |k|; fp16/bf16 output
   within 1 ulp of the larger of the two values, plus the same 2e-6 x row-max
   floor (below it the fp32 rotation's own rounding decides the last bit);
-* fetched V: bit-exact, except FP8-sourced V rounded to fp16/bf16, where the
-  fp32 dequantized value is rounded a second time (within 1 ulp);
+* fetched V: bit-exact, except FP8-sourced V (either FP8 wire) rounded to
+  fp16/bf16, where the fp32 dequantized value is rounded a second time
+  (within 1 ulp);
 * every element the fetch must not touch keeps its sentinel, bit for bit.
 """
 from dataclasses import dataclass
@@ -88,6 +89,9 @@ def oracle_run(c, wire, group=32, scale_dtype="f16"):
     elif wire == "int4":
         codes, scales = paged.encode_int4(c.src_k, c.src_v, c.src_slots, c.n_valid, group, scale_dtype)
         vals = paged.decode_int4(codes, scales, group)
+    elif wire == "fp8_rows":
+        codes, scales = paged.encode_fp8_rows(c.src_k, c.src_v, c.src_slots, c.n_valid, scale_dtype)
+        vals = paged.decode_fp8_rows(codes, scales)
     else:
         codes, scales = None, None
         vals = paged.gather_slabs(c.src_k, c.src_v, c.src_slots)
@@ -162,7 +166,7 @@ def compare_outputs(c, wire, gout, oout):
     rep.update(k_ok=ok_k, k_max_err=kerr, k_bar=kbar)
     gv, ev = gout["v"][m], oout["v"][m]
     rep["v_exact"] = bool(np.array_equal(gv, ev))
-    if wire == "fp8" and c.out_fmt != "f32":
+    if wire in ("fp8", "fp8_rows") and c.out_fmt != "f32":
         rep["v_ok"] = bool(np.all(np.abs(gv - ev) <= np.maximum(ulp(gv, c.out_fmt), ulp(ev, c.out_fmt))))
     else:
         rep["v_ok"] = rep["v_exact"]

@@ -27,10 +27,10 @@ def lib():
     return hc.lib()
 
 
-def test_header_declares_the_four_calls():
+def test_header_declares_the_calls():
     names = _declared_functions()
-    for n in ("hc_encode_fp8", "hc_encode_int4", "hc_build_delta_sincos",
-              "hc_fetch_rotate_scatter", "hc_status_string"):
+    for n in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
+              "hc_fetch_rotate_scatter", "hc_crc32", "hc_status_string"):
         assert n in names, names
 
 
@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     from kv_cache_quantization_hc_gb300 import hc
-    assert hc.hc_version() == 1
+    assert hc.hc_version() == 2
     assert hc.status_string(0) == "HC_OK"
     assert hc.status_string(-1) == "HC_ERR_INVALID_ARG"
     assert hc.status_string(-2) == "HC_ERR_UNSUPPORTED"
@@ -89,3 +89,26 @@ def test_host_validation_without_cuda(lib):
     assert L.hc_encode_fp8(A, A, P(good), A, None, 0, A, A, A, None) == hc.HC_OK
     assert f(0, A, A, 32, hc.HC_F16, A, A, 0, 0, A, None, 0, A, A, P(good), A, None) == hc.HC_OK
     assert t(A, 0, 128, ctypes.c_double(1e4), None, A, None) == hc.HC_OK
+
+
+def test_host_validation_of_rows_and_crc(lib):
+    """Row-scaled FP8 and CRC-32 argument checks (fake addresses, no CUDA)."""
+    from kv_cache_quantization_hc_gb300 import hc
+    A = 1 << 20
+    good = hc.hc_paged_desc(1, 8, 128, 16, 4, hc.HC_BF16, 16 * 8 * 128, 0)
+    P = ctypes.byref
+    r = lib.hc_encode_fp8_rows
+    assert r(A, A, P(good), A, None, 1, 7, A, A, A, None) == hc.HC_ERR_INVALID_ARG      # scale dtype
+    assert r(A, A, P(good), A, None, 1, hc.HC_F16, A + 8, A, A, None) == hc.HC_ERR_INVALID_ARG  # codes
+    assert r(A, A, P(good), A, None, 1, hc.HC_F16, A, A + 1, A, None) == hc.HC_ERR_INVALID_ARG  # scales
+    assert r(A, A, P(good), A, None, 0, hc.HC_F16, A, A, A, None) == hc.HC_OK
+    f = lib.hc_fetch_rotate_scatter
+    assert f(3, A, A, 32, 9, A, A, 1, 0, A, None, 1, A, A, P(good), A, None) == hc.HC_ERR_INVALID_ARG
+    assert f(3, A, A + 2, 32, hc.HC_F32, A, A, 1, 0, A, None, 1, A, A, P(good), A, None) == hc.HC_ERR_INVALID_ARG
+    c = lib.hc_crc32
+    assert c(A + 4, 64, 64, None, 0, 0, 1, A, None) == hc.HC_ERR_INVALID_ARG          # a alignment
+    assert c(A, 64, 72, None, 0, 0, 2, A, None) == hc.HC_ERR_INVALID_ARG              # a stride
+    assert c(A, 64, 32, None, 0, 0, 2, A, None) == hc.HC_ERR_INVALID_ARG              # overlap
+    assert c(A, 64, 64, None, 8, 8, 1, A, None) == hc.HC_ERR_INVALID_ARG              # b missing
+    assert c(A, 64, 64, None, 0, 0, -1, A, None) == hc.HC_ERR_INVALID_ARG
+    assert c(A, 64, 64, None, 0, 0, 0, A, None) == hc.HC_OK

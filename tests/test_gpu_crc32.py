@@ -1,0 +1,87 @@
+"""GPU parity of the CRC-32 kernel (hc_crc32) against the oracle's CRC-32,
+on random units of many sizes and on encoded wire buffers, plus tamper
+detection: changing one byte of a unit changes that unit's CRC only."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import crc32 as ocrc
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+# a_bytes, a_stride, b_bytes, b_stride, n_units
+SHAPES = [(0, 0, 0, 0, 3), (0, 16, 5, 7, 4), (1, 16, 0, 0, 5), (15, 16, 3, 3, 2),
+          (16, 32, 0, 0, 9), (4095, 4096, 1, 1, 3), (4096, 4096, 64, 64, 17),
+          (4096 + 48, 4160, 13, 20, 6), (32768, 32768, 64, 64, 40), (65536 + 16, 65552, 0, 0, 3),
+          (131072, 131072, 2048, 2048, 2)]
+
+
+@pytest.mark.parametrize("a_bytes,a_stride,b_bytes,b_stride,n", SHAPES)
+def test_crc32_units(a_bytes, a_stride, b_bytes, b_stride, n):
+    from kv_cache_quantization_hc_gb300 import hc
+    r = np.random.default_rng(a_bytes * 7 + n)
+    a = r.integers(0, 256, max(a_stride * n, 16), dtype=np.uint8)
+    b = r.integers(0, 256, max(b_stride * n, b_bytes, 1), dtype=np.uint8)
+    da, db = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    out = torch.zeros(n, dtype=torch.int32, device=DEV)
+    hc.hc_crc32(da, a_bytes, a_stride, db if b_bytes else None, b_bytes, b_stride, n, out)
+    torch.cuda.synchronize()
+    want = ocrc.crc32_units(a, a_bytes, a_stride, n, b if b_bytes else None, b_bytes, b_stride)
+    assert np.array_equal(_u32(out), want)
+
+
+def test_crc32_check_value():
+    from kv_cache_quantization_hc_gb300 import hc
+    msg = torch.tensor(list(b"123456789") + [0] * 7, dtype=torch.uint8, device=DEV)
+    out = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hc.hc_crc32(msg, 9, 16, None, 0, 0, 1, out)
+    assert _u32(out)[0] == 0xCBF43926
+
+
+@pytest.mark.parametrize("wire", ["fp8", "int4", "fp8_rows"])
+def test_crc32_of_the_wire_and_tamper_detection(wire):
+    """Per (layer, block): CRC of its codes followed by its scales, on the GPU
+    wire, equals the oracle's CRC of the oracle's wire (the two wires are
+    bit-identical); one flipped byte changes exactly one unit's CRC."""
+    from kv_cache_quantization_hc_gb300 import path as kvpath
+    c = parity.random_case(61, L=3, H=4, d=128, B=16, nb=5, src_fmt="bf16", out_fmt="bf16",
+                           ragged=True)
+    o = parity.oracle_run(c, wire, scale_dtype="f16")
+    dm_vals, dm_idx = np.unique(c.delta_m, return_inverse=True)
+    p = kvpath.KVPath(n_layers=c.L, H=c.H, d=c.d, B=c.B, n_blocks=len(c.src_slots),
+                      src_slots=c.src_slots, dst_slots=c.dst_slots, n_valid=c.n_valid,
+                      delta_m_distinct=dm_vals, delta_idx=dm_idx, wire=wire, pairing=c.pairing,
+                      rope_base=c.rope_base, paged_dtype=c.out_fmt, scale_dtype="f16")
+    src_k = torch.as_tensor(c.src_k, device=DEV).to(torch.bfloat16)
+    src_v = torch.as_tensor(c.src_v, device=DEV).to(torch.bfloat16)
+    p.encode(src_k, src_v)
+    got = _u32(p.crc32())
+    codes = o["codes"]
+    sdt = np.float32 if wire == "fp8" else np.float16
+    scales = o["scales"].astype(sdt)
+    L, NB = c.L, len(c.src_slots)
+    a = codes.reshape(L * NB, -1)
+    bb = scales.reshape(L * NB, -1).view(np.uint8)
+    want = ocrc.crc32_units(a, a.shape[1], a.shape[1], L * NB, bb, bb.shape[1], bb.shape[1])
+    assert np.array_equal(got, want)
+    # tamper: flip one byte of unit (layer 1, block 3)
+    u = 1 * NB + 3
+    flat = p.codes.view(-1)
+    i = u * a.shape[1] + 777
+    flat[i] = flat[i] ^ 0x10
+    got2 = _u32(p.crc32())
+    changed = np.nonzero(got2 != got)[0]
+    assert changed.tolist() == [u]

@@ -7,7 +7,8 @@ and scales the C-ABI kernels write are compared, bit for bit, with IEEE fp32
 arithmetic done by torch on the GPU:
 
   FP8:  s = fp32(a / 448),  code = float8_e4m3fn(fp32(x / s))  (RNE; |q| stays
-        below 464, so the cast needs no saturation)
+        below 464, so the cast needs no saturation); per slab, and per row
+        with fp16 or fp32 scales
   INT4: s = fp16(fp32(a / 7)), code = round_half_even(fp32(x / s)) in [-7, 7]
         (an fp16 scale that overflows to +inf gives x / s = 0)
 
@@ -144,4 +145,53 @@ def test_fp8_all_pairs(fmt):
         assert not bool(bad.any()), (fmt, int(bad.sum()))
         assert torch.equal(scales[0, :, 0], s[..., 0])
         checked += ns * (slab - 1)
+    assert checked > 1.0e9
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+@pytest.mark.parametrize("scale", ["f16", "f32"])
+def test_fp8_rows_all_pairs(fmt, scale):
+    """Row-scaled FP8: each (token, head) row of 128 channels holds one amax
+    and 127 values x with |x| <= amax.  Reference: s32 = fp32(a / 448), s =
+    fp16(s32) or s32, code = float8_e4m3fn(clamp(fp32(x / s), +-448)): an
+    fp16-subnormal scale can be well below a / 448, and torch's cast turns
+    values past 448 into NaN, so the reference saturates first (clamping, then
+    rounding, is the satfinite rounding).  A scale of 0 gives codes 0, a scale
+    that overflows fp16 (+inf) gives the codes of x / inf = +-0."""
+    from kv_cache_quantization_hc_gb300 import hc
+    mags = _magnitudes(fmt)
+    B, H, d = 16, 8, 128
+    per_slot = B * H
+    checked = 0
+    for ia0, ia1 in _chunks(len(mags), 2048):
+        grp = _pairs(mags, ia0, ia1, d)                         # one row per group
+        nr = grp.shape[0]
+        nslots = (nr + per_slot - 1) // per_slot
+        flat = torch.zeros((nslots * per_slot, d), device=DEV)
+        flat[:nr] = grp
+        del grp
+        src = flat.to(TDT[fmt]).reshape(1, nslots, B, H, d)     # row (slot, t, h)
+        codes = torch.empty((1, nslots, 2, H, B, d), dtype=torch.uint8, device=DEV)
+        sdt = torch.float16 if scale == "f16" else torch.float32
+        scales = torch.empty((1, nslots, 2, H, B), dtype=sdt, device=DEV)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        slots = torch.arange(nslots, dtype=torch.int32, device=DEV)
+        hc.hc_encode_fp8_rows(src, src, hc.paged_desc(src), slots, None, nslots,
+                              hc.HC_F16 if scale == "f16" else hc.HC_F32, codes, scales, err)
+        x = src.float().reshape(nslots, B, H, d)
+        am = x.abs().amax(-1, keepdim=True)
+        s = am / torch.full_like(am, 448.0)                   # tensor / tensor: IEEE division
+        if scale == "f16":
+            s = s.half().float()
+        q = torch.where(s > 0, x / s, torch.zeros_like(x)).clamp(-448.0, 448.0)
+        want = q.to(torch.float8_e4m3fn).view(torch.uint8)
+        want = torch.where(s > 0, want, torch.zeros_like(want))
+        got = codes[0, :, 0].permute(0, 2, 1, 3)                # [slot, t, h, d]
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        bad = (got != want).reshape(-1, d)[:nr].any(-1)
+        assert not bool(bad.any()), (fmt, scale, int(bad.sum()))
+        got_s = scales[0, :, 0].permute(0, 2, 1).float()        # [slot, t, h]
+        assert torch.equal(got_s, s[..., 0])
+        checked += nr * (d - 1)
     assert checked > 1.0e9
