@@ -267,7 +267,8 @@ def run_ours(args):
     crc = run_crc(args, p, device) if args.crc else None
     e2e = None
     if "e2e" in args.legs:
-        e2e = run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device)
+        e2e = run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device,
+                      device_step_s=total_s / args.steps)
     cpu = None
     if "cpu" in args.legs and rank == 0 and world == 1:
         cpu = cpu_baseline(w, blk, budget_s=args.cpu_seconds)
@@ -333,13 +334,16 @@ def run_crc(args, p, device):
             "bound": "hbm (read only)"}
 
 
-def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device):
+def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device, device_step_s=None):
     """Same step through the C ABI with host buffers, layer-streamed (the
     public LayerStream schedule): per layer, the fp16 source is copied from
     pinned host memory, encoded and fetched, and the bf16 result copied back;
     uploads, kernels and downloads of neighbouring layers overlap on three
     streams.  The block tables are uploaded every step as well.  Every copy is
-    inside the timed region."""
+    inside the timed region.  `overlap` compares the step with its parts run
+    alone (whole upload, the device step, whole download): hidden_frac is the
+    share of the shorter parts' time that the pipeline hid (1 = the step takes
+    only as long as its longest part)."""
     import copy
     import torch
     from kv_cache_quantization_hc_gb300 import path as kvpath
@@ -382,9 +386,30 @@ def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device):
     if int(h_err.item()):
         raise RuntimeError("device error flag set in e2e leg")
     secs, total = reduce_max_sum(a.elapsed_time(b) / 1e3, step_bytes * steps)
+    overlap = None
+    if device_step_s:
+        # each part alone: the whole source up, the whole result down
+        def alone(fn):
+            fn()
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            return e0.elapsed_time(e1) / 1e3
+        up = alone(lambda: (src_k.copy_(h_src_k, non_blocking=True), src_v.copy_(h_src_v, non_blocking=True)))
+        down = alone(lambda: (h_dst_k.copy_(dst_k, non_blocking=True), h_dst_v.copy_(dst_v, non_blocking=True)))
+        serial = up + device_step_s + down
+        e2e_s = secs / steps
+        longest = max(up, device_step_s, down)
+        overlap = {"upload_ms": up * 1e3, "compute_ms": device_step_s * 1e3, "download_ms": down * 1e3,
+                   "serial_ms": serial * 1e3, "e2e_ms": e2e_s * 1e3,
+                   "hidden_frac": (serial - e2e_s) / (serial - longest) if serial > longest else None}
     return {"value": total / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3,
-            "schedule": "layer-streamed: upload l+1 / compute l / download l-1 on three streams"}
+            "schedule": "layer-streamed: upload l+1 / compute l / download l-1 on three streams",
+            "overlap": overlap}
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -579,6 +604,60 @@ def run_layered(args):
         "clocks": clocks.summary()}))
 
 
+def run_blend(args):
+    """Drift-ranked token selection on 64 sequences x 2048 tokens x hidden 4096
+    (bf16): drift of every token (both hidden-state arrays read once) and the
+    top-15% selection per sequence, one hc_drift_select call per step."""
+    import torch
+    import __graft_entry__
+    import workloads
+    from oracle import blend
+    from kv_cache_quantization_hc_gb300 import hc
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+    w = workloads.blend_selection()
+    cached, fresh = workloads.blend_hidden(w, device)
+    k = blend.default_k(w.n_tokens)
+    drift = torch.empty((w.n_seq, w.n_tokens), dtype=torch.float32, device=device)
+    sel = torch.empty((w.n_seq, k), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    es = cached.element_size()
+    nbytes = 2 * cached.numel() * es + drift.numel() * 4 + sel.numel() * 4
+    for _ in range(max(args.warmup, 3)):
+        hc.drift_select(cached, fresh, k, drift, sel, stream)
+    torch.cuda.synchronize(device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize(device)
+        for a, b in evs:
+            a.record(stream)
+            hc.drift_select(cached, fresh, k, drift, sel, stream)
+            b.record(stream)
+        torch.cuda.synchronize(device)
+    times = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    avg = statistics.mean(times)
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({
+        "metric": "drift-ranked token selection GB/s (layer-0 hidden states read once)",
+        "value": nbytes / avg / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": avg * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.n_seq} sequences x {w.n_tokens} tokens x hidden "
+                               f"{w.hidden}, {w.dtype}, k = {k} (ceil 15%)",
+                   "bytes_per_step": nbytes,
+                   "l2": "inputs larger than L2 (%.2f GB per step)" % (nbytes / 1e9)},
+        "tokens_per_s": w.n_seq * w.n_tokens / avg,
+        "roofline": {"kernel": "k_drift + k_select", "bound": "hbm", "achieved": nbytes / avg / 1e9,
+                     "peak": peak, "unit": "GB/s", "frac": nbytes / avg / 1e9 / peak, "traffic": None,
+                     "peak_source": peak_kind},
+        "gpu_launches": 2 * args.steps, "min_ms": min(times) * 1e3,
+        "clocks": clocks.summary()}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -586,9 +665,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a smaller case)")
-    ap.add_argument("--workload", choices=["qwen3_8b", "llama3_70b", "ragged"], default="qwen3_8b",
-                    help="qwen3_8b: the step the JSON line reports by default; the others time the "
-                         "per-layer calls of the layer-streamed and ragged workloads")
+    ap.add_argument("--workload", choices=["qwen3_8b", "llama3_70b", "ragged", "blend"],
+                    default="qwen3_8b",
+                    help="qwen3_8b: the step the JSON line reports by default; llama3_70b / ragged "
+                         "time the per-layer calls of the layer-streamed and ragged workloads; blend "
+                         "times the drift-ranked token selection")
     ap.add_argument("--legs", default="device,e2e,cpu", help="comma list of: device, e2e, cpu")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -603,6 +684,8 @@ def main(argv=None):
     args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "blend":
+        run_blend(args)
     elif args.workload != "qwen3_8b":
         run_layered(args)
     else:

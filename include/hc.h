@@ -233,6 +233,34 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
 int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, int64_t b_bytes,
              int64_t b_stride, int32_t n_units, uint32_t* crc, void* stream);
 
+/* hc_drift_select: the tokens to recompute after cached chunks are reordered.
+ * Layer-0 K/V depends only on the token embeddings, so the rotated layer-0 KV
+ * is exact; the tokens whose layer-0 hidden state drifted most are recomputed
+ * through the deeper layers.  For each sequence s < n_seq and token t:
+ *   drift[s][t] = sqrt( sum_c (h_fresh[s][t][c] - h_cached[s][t][c])^2 )
+ * (differences, squares and the sum in fp32; the sum's order is the
+ * library's), and selected[s][0..k) = the k tokens with the largest drift,
+ * ties to the lower index, in ascending order.  The caller picks k; about 15%
+ * of the tokens is the page's figure.
+ * [HyperCache page, "Core Design", selective recomputation ("top ~15% of
+ *  tokens with the largest Layer-0 hidden-state drift", CacheBlend).]
+ *
+ *   h_cached, h_fresh : device, dtype f32/f16/bf16, 16-byte aligned; element
+ *                       (s, t, c) at base + s*seq_stride + t*token_stride + c
+ *   n_seq        : >= 0; 0 launches nothing.  n_seq * n_tokens < 2^31
+ *   n_tokens     : >= 1
+ *   hidden       : a multiple of 8, >= 8
+ *   token_stride : >= hidden; seq_stride >= n_tokens * token_stride when
+ *                  n_seq > 1; both in elements, times the element size a
+ *                  multiple of 16 bytes
+ *   k            : 1 <= k <= n_tokens
+ *   drift        : device f32 [n_seq][n_tokens], written in full
+ *   selected     : device int32 [n_seq][k], written in full
+ * Hidden states must be finite.  Returns HC_OK, HC_ERR_INVALID_ARG or HC_ERR_CUDA. */
+int hc_drift_select(const void* h_cached, const void* h_fresh, int32_t dtype, int32_t n_seq,
+                    int32_t n_tokens, int32_t hidden, int64_t token_stride, int64_t seq_stride,
+                    int32_t k, float* drift, int32_t* selected, void* stream);
+
 /* Human-readable name of an hc_status value (static string, never NULL). */
 const char* hc_status_string(int32_t status);
 

@@ -256,6 +256,34 @@ int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, in
   return record(hc::launch_crc32(p, static_cast<cudaStream_t>(stream)));
 }
 
+int hc_drift_select(const void* h_cached, const void* h_fresh, int32_t dtype, int32_t n_seq,
+                    int32_t n_tokens, int32_t hidden, int64_t token_stride, int64_t seq_stride,
+                    int32_t k, float* drift, int32_t* selected, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0 || n_seq < 0 || n_tokens < 1 || hidden < 8 || hidden % 8) return HC_ERR_INVALID_ARG;
+  if (k < 1 || k > n_tokens) return HC_ERR_INVALID_ARG;
+  if (!h_cached || !h_fresh || !drift || !selected) return HC_ERR_INVALID_ARG;
+  if (token_stride < hidden || (n_seq > 1 && seq_stride < int64_t{n_tokens} * token_stride))
+    return HC_ERR_INVALID_ARG;
+  if ((token_stride * es) % 16 || (seq_stride * es) % 16 || seq_stride < 0) return HC_ERR_INVALID_ARG;
+  if (!aligned(h_cached, 16) || !aligned(h_fresh, 16) || !aligned(drift, 4) || !aligned(selected, 4))
+    return HC_ERR_INVALID_ARG;
+  if (int64_t{n_seq} * n_tokens >= (int64_t{1} << 31)) return HC_ERR_INVALID_ARG;
+  if (n_seq == 0) return HC_OK;
+  hc::SelectParams p;
+  p.cached = h_cached;
+  p.fresh = h_fresh;
+  p.token_stride = token_stride;
+  p.seq_stride = seq_stride;
+  p.n_seq = n_seq;
+  p.n_tokens = n_tokens;
+  p.hidden = hidden;
+  p.k = k;
+  p.drift = drift;
+  p.selected = selected;
+  return record(hc::launch_drift_select(dtype, p, static_cast<cudaStream_t>(stream)));
+}
+
 const char* hc_status_string(int32_t status) {
   switch (status) {
     case HC_OK: return "HC_OK";

@@ -103,6 +103,17 @@ struct CrcParams {
   uint32_t init_term;
 };
 
+// Drift-ranked token selection over n_seq sequences of n_tokens rows of
+// `hidden` elements (strides in elements).
+struct SelectParams {
+  const void* cached;
+  const void* fresh;
+  int64_t token_stride, seq_stride;
+  int32_t n_seq, n_tokens, hidden, k;
+  float* drift;       // [n_seq][n_tokens]
+  int32_t* selected;  // [n_seq][k]
+};
+
 // Launchers: return the launch's cudaError_t.  `dtype`/`out_dtype` are hc_dtype.
 cudaError_t launch_encode_fp8(int dtype, int d, const EncodeParams& p, cudaStream_t s);
 cudaError_t launch_encode_fp8_rows(int dtype, int d, bool scale_f16, const EncodeParams& p,
@@ -110,6 +121,7 @@ cudaError_t launch_encode_fp8_rows(int dtype, int d, bool scale_f16, const Encod
 cudaError_t launch_fetch_fp8_rows(int out_dtype, int d, bool half_split, bool scale_f16,
                                   const FetchParams& p, cudaStream_t s);
 cudaError_t launch_crc32(const CrcParams& p, cudaStream_t s);
+cudaError_t launch_drift_select(int dtype, const SelectParams& p, cudaStream_t s);
 cudaError_t launch_encode_int4(int dtype, int d, bool scale_f16, const EncodeParams& p,
                                cudaStream_t s);
 cudaError_t launch_fetch_fp8(int out_dtype, int d, bool half_split, const FetchParams& p,

@@ -57,8 +57,9 @@ def lib():
                                               _I32, _P, _P, desc_p, _P, _P]
         _I64 = ctypes.c_int64
         L.hc_crc32.argtypes = [_P, _I64, _I64, _P, _I64, _I64, _I32, _P, _P]
+        L.hc_drift_select.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I64, _I64, _I32, _P, _P, _P]
         for fn in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
-                   "hc_fetch_rotate_scatter", "hc_crc32"):
+                   "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select"):
             getattr(L, fn).restype = ctypes.c_int
         L.hc_status_string.argtypes = [_I32]
         L.hc_status_string.restype = ctypes.c_char_p
@@ -146,6 +147,34 @@ def hc_crc32(a, a_bytes, a_stride, b, b_bytes, b_stride, n_units, crc, stream=No
     _check("hc_crc32", lib().hc_crc32(
         _ptr(a), a_bytes, a_stride, _ptr(b), b_bytes, b_stride, n_units, _ptr(crc),
         _stream(stream)))
+
+
+def hc_drift_select(h_cached, h_fresh, dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
+                    drift, selected, stream=None):
+    _check("hc_drift_select", lib().hc_drift_select(
+        _ptr(h_cached), _ptr(h_fresh), dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
+        _ptr(drift), _ptr(selected), _stream(stream)))
+
+
+def drift_select(h_cached, h_fresh, k, drift=None, selected=None, stream=None):
+    """hc_drift_select on tensors shaped [n_seq, n_tokens, hidden] (or
+    [n_tokens, hidden]); returns (drift [n_seq, n_tokens] f32, selected
+    [n_seq, k] int32)."""
+    import torch
+    if h_cached.dim() == 2:
+        h_cached, h_fresh = h_cached.unsqueeze(0), h_fresh.unsqueeze(0)
+    if h_cached.shape != h_fresh.shape or h_cached.stride() != h_fresh.stride():
+        raise ValueError("h_cached and h_fresh must have the same shape and strides")
+    if h_cached.stride(2) != 1:
+        raise ValueError("the hidden dimension must be contiguous")
+    n_seq, n_tokens, hidden = h_cached.shape
+    dev = h_cached.device
+    drift = torch.empty((n_seq, n_tokens), dtype=torch.float32, device=dev) if drift is None else drift
+    selected = torch.empty((n_seq, k), dtype=torch.int32, device=dev) if selected is None else selected
+    dtype = {"torch.float32": HC_F32, "torch.float16": HC_F16, "torch.bfloat16": HC_BF16}[str(h_cached.dtype)]
+    hc_drift_select(h_cached, h_fresh, dtype, n_seq, n_tokens, hidden, h_cached.stride(1),
+                    h_cached.stride(0), k, drift, selected, stream)
+    return drift, selected
 
 
 def hc_build_delta_sincos(delta_m, n_distinct, d_head, rope_base, inv_freq, table, stream=None):

@@ -30,7 +30,7 @@ def lib():
 def test_header_declares_the_calls():
     names = _declared_functions()
     for n in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
-              "hc_fetch_rotate_scatter", "hc_crc32", "hc_status_string"):
+              "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select", "hc_status_string"):
         assert n in names, names
 
 
@@ -112,3 +112,18 @@ def test_host_validation_of_rows_and_crc(lib):
     assert c(A, 64, 64, None, 8, 8, 1, A, None) == hc.HC_ERR_INVALID_ARG              # b missing
     assert c(A, 64, 64, None, 0, 0, -1, A, None) == hc.HC_ERR_INVALID_ARG
     assert c(A, 64, 64, None, 0, 0, 0, A, None) == hc.HC_OK
+
+
+def test_host_validation_of_drift_select(lib):
+    from kv_cache_quantization_hc_gb300 import hc
+    A = 1 << 20
+    d = lib.hc_drift_select
+    ok = (A, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 15, A, A, None)
+    assert d(*ok[:2], 9, *ok[3:]) == hc.HC_ERR_INVALID_ARG                       # dtype
+    assert d(A, A, hc.HC_BF16, 2, 100, 60, 64, 6400, 15, A, A, None) == hc.HC_ERR_INVALID_ARG   # hidden % 8
+    assert d(A, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 0, A, A, None) == hc.HC_ERR_INVALID_ARG    # k = 0
+    assert d(A, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 101, A, A, None) == hc.HC_ERR_INVALID_ARG  # k > T
+    assert d(A, A, hc.HC_BF16, 2, 100, 64, 60, 6400, 15, A, A, None) == hc.HC_ERR_INVALID_ARG   # stride
+    assert d(A, A, hc.HC_BF16, 2, 100, 64, 64, 6000, 15, A, A, None) == hc.HC_ERR_INVALID_ARG   # overlap
+    assert d(A + 8, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 15, A, A, None) == hc.HC_ERR_INVALID_ARG
+    assert d(A, A, hc.HC_BF16, 0, 100, 64, 64, 6400, 15, A, A, None) == hc.HC_OK

@@ -252,3 +252,48 @@ def device_pool(w, blk, layers, kv, device, seed_offset=0):
             raise ValueError(dist)
         out[i] = x.to(dt)
     return out
+
+
+# ------------------------------------------------------------------ token selection
+@dataclass
+class BlendWorkload:
+    """Layer-0 hidden states before (cached) and after (fresh) a reorder, for
+    the drift-ranked token selection: n_seq sequences of n_tokens rows of
+    `hidden` values.  cached ~ N(0, 1); fresh = cached + delta with
+    delta_t ~ N(0, sigma_t^2), sigma_t = 0.05 * exp(N(0, 1)) per token (a
+    heavy-tailed spread of drifts, so the top 15% is a real selection)."""
+    name: str
+    n_seq: int
+    n_tokens: int
+    hidden: int
+    dtype: str
+    seed: int
+    fraction: float = 0.15
+
+
+def blend_selection(seed=5):
+    """64 sequences x 2048 tokens x hidden 4096 (the Qwen3-8B hidden size), bf16."""
+    return BlendWorkload("blend_selection", 64, 2048, 4096, "bf16", seed)
+
+
+def blend_small(seed=6):
+    return BlendWorkload("blend_small", 3, 1408, 256, "bf16", seed)
+
+
+def blend_hidden(w, device, seqs=None):
+    """(cached, fresh) [len(seqs), n_tokens, hidden] drawn on `device`; each
+    sequence has its own generator seed, so any sequence can be re-drawn."""
+    import torch
+    seqs = range(w.n_seq) if seqs is None else seqs
+    dt = torch_dtype(w.dtype)
+    cached = torch.empty((len(seqs), w.n_tokens, w.hidden), dtype=dt, device=device)
+    fresh = torch.empty_like(cached)
+    for i, s in enumerate(seqs):
+        g = torch.Generator(device=device)
+        g.manual_seed(w.seed * 1_000_003 + s)
+        c = torch.randn((w.n_tokens, w.hidden), generator=g, device=device, dtype=torch.float32)
+        sigma = 0.05 * torch.exp(torch.randn((w.n_tokens, 1), generator=g, device=device))
+        d = torch.randn((w.n_tokens, w.hidden), generator=g, device=device, dtype=torch.float32) * sigma
+        cached[i] = c.to(dt)
+        fresh[i] = (c + d).to(dt)
+    return cached, fresh
