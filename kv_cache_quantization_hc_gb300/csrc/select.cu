@@ -13,8 +13,9 @@
 // k_drift: one warp per token row, 16-byte loads of both rows, an fma per
 // element, a fixed shuffle tree.  k_select: one CTA per sequence.  The drift
 // values are non-negative, so their fp32 bit patterns order like the values:
-// a radix select over the four key bytes (shared-memory histograms) finds the
-// k-th largest key tau and how many keys equal to tau belong to the top k;
+// a radix select over the four key bytes (shared-memory histograms, the bin
+// found by one warp's scan) finds the k-th largest key tau and how many keys
+// equal to tau belong to the top k;
 // two block-wide scans then write, in index order, every token above tau and
 // the first such number of tokens equal to it.
 #include "hc_internal.cuh"
@@ -93,15 +94,35 @@ __global__ void __launch_bounds__(kSelectThreads) k_select(SelectParams p) {
       if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 0xffu], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t above = 0;
-      for (int bin = 255; bin >= 0; --bin) {
-        if (above + hist[bin] >= left) {
-          s_prefix = prefix | (static_cast<uint32_t>(bin) << shift);
-          s_left = left - above;
-          break;
+    if (threadIdx.x < 32) {
+      // warp 0: lane l holds bins 255 - 8l down to 248 - 8l; a scan over
+      // the lanes' totals (highest bins first) finds the lane, then the bin
+      const int lane = threadIdx.x;
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * lane - i];
+        tot += c[i];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      const uint32_t above_lane = incl - tot;  // keys in higher bins than this lane's
+      const uint32_t hit = __ballot_sync(0xffffffffu, above_lane < left && incl >= left);
+      if (lane == __ffs(hit) - 1) {
+        uint32_t above = above_lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + c[i] >= left) {
+            s_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - i) << shift);
+            s_left = left - above;
+            break;
+          }
+          above += c[i];
         }
-        above += hist[bin];
       }
     }
     __syncthreads();

@@ -39,6 +39,9 @@ def _check_blocks(w, blk, js, layers, src_k_host, src_v_host, codes, scales, dst
     if wire == "fp8":
         ocodes, oscales = paged.encode_fp8(src_k_host, src_v_host, np.arange(n), nv)
         vals = paged.decode_fp8(ocodes, oscales)
+    elif wire == "fp8_rows":
+        ocodes, oscales = paged.encode_fp8_rows(src_k_host, src_v_host, np.arange(n), nv, scale_dtype)
+        vals = paged.decode_fp8_rows(ocodes, oscales)
     else:
         ocodes, oscales = paged.encode_int4(src_k_host, src_v_host, np.arange(n), nv, group, scale_dtype)
         vals = paged.decode_int4(ocodes, oscales, group)
@@ -54,19 +57,20 @@ def _check_blocks(w, blk, js, layers, src_k_host, src_v_host, codes, scales, dst
     ok_k, kerr, kbar = parity.compare_k(dst_k[m], ek[m], w.out_dtype)
     assert ok_k, (kerr, kbar)
     gv, evv = dst_v[m], ev[m]
-    if wire == "fp8" and w.out_dtype != "f32":
+    if wire in ("fp8", "fp8_rows") and w.out_dtype != "f32":
         assert np.all(np.abs(gv - evv) <= np.maximum(parity.ulp(gv, w.out_dtype), parity.ulp(evv, w.out_dtype)))
     else:
         assert np.array_equal(gv, evv)
     return m
 
 
-def test_qwen3_8b_benchmark_step():
+@pytest.mark.parametrize("codec", ["fp8", "fp8_rows"])
+def test_qwen3_8b_benchmark_step(codec):
     import bench
     dev = torch.device("cuda", 0)
     w = workloads.qwen3_8b()
     blk = w.blocks[0]
-    p, src_k, src_v, dst_k, dst_v = bench.setup_device(w, blk, dev)
+    p, src_k, src_v, dst_k, dst_v = bench.setup_device(w, blk, dev, codec)
     dst_k.fill_(float("nan"))
     dst_v.fill_(float("nan"))
     p.encode(src_k, src_v)
@@ -89,7 +93,7 @@ def test_qwen3_8b_benchmark_step():
     host = lambda t: t.double().cpu().numpy()
     _check_blocks(w, blk, js, range(w.L), host(src_k[:, sl]), host(src_v[:, sl]),
                   p.codes[:, js].cpu().numpy(), host(p.scales[:, js]), host(dst_k[:, dl]),
-                  host(dst_v[:, dl]), "fp8")
+                  host(dst_v[:, dl]), codec)
 
 
 def test_llama3_70b_layer_streamed():
