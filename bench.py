@@ -658,6 +658,42 @@ def run_blend(args):
         "clocks": clocks.summary()}))
 
 
+def run_hashing(args):
+    """Host-side block digests (hc_block_digests, one core): the prefix and
+    content BLAKE2b-128 digests of 445,722 token ids in blocks of 16 and of
+    64, per tenant key; the oracle (hashlib) timed beside it."""
+    from kv_cache_quantization_hc_gb300 import hc
+    from oracle import hashing
+    import __graft_entry__
+    __graft_entry__.build()
+    r = np.random.default_rng(7)
+    tokens = r.integers(0, 151936, 445722).astype(np.int32)     # a Qwen3-sized vocabulary
+    key = hc.tenant_key(b"bench master secret", "tenant-0")
+    out = {}
+    for B in (16, 64):
+        hc.block_digests(tokens, B, key)
+        reps = max(1, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            hc.block_digests(tokens, B, key)
+        dt = (time.perf_counter() - t0) / reps
+        n_blocks = -(-len(tokens) // B)
+        sample = tokens[: 64 * B]
+        t1 = time.perf_counter()
+        hashing.block_digests(sample, B, key)
+        dto = (time.perf_counter() - t1) * len(tokens) / len(sample)
+        out[f"B{B}"] = {"blocks_per_s": n_blocks / dt, "ms_per_pass": dt * 1e3,
+                        "token_bytes_per_s": 4 * len(tokens) / dt,
+                        "oracle_blocks_per_s": n_blocks / dto}
+    print(json.dumps({
+        "metric": "block digests per second (host, one core; two BLAKE2b-128 per block)",
+        "value": out["B16"]["blocks_per_s"], "unit": "blocks/s", "n_gpus": 0, "steps": reps,
+        "higher_is_better": True, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "445,722 token ids (vocabulary 151,936), blocks of 16 and 64, "
+                               "tenant-keyed prefix and content digests"},
+        "blocks": out, "cores": 1}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -665,11 +701,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a smaller case)")
-    ap.add_argument("--workload", choices=["qwen3_8b", "llama3_70b", "ragged", "blend"],
+    ap.add_argument("--workload", choices=["qwen3_8b", "llama3_70b", "ragged", "blend", "hashing"],
                     default="qwen3_8b",
                     help="qwen3_8b: the step the JSON line reports by default; llama3_70b / ragged "
                          "time the per-layer calls of the layer-streamed and ragged workloads; blend "
-                         "times the drift-ranked token selection")
+                         "times the drift-ranked token selection; hashing the host-side block "
+                         "digests")
     ap.add_argument("--legs", default="device,e2e,cpu", help="comma list of: device, e2e, cpu")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -686,6 +723,8 @@ def main(argv=None):
         run_reference(args)
     elif args.workload == "blend":
         run_blend(args)
+    elif args.workload == "hashing":
+        run_hashing(args)
     elif args.workload != "qwen3_8b":
         run_layered(args)
     else:

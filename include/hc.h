@@ -261,6 +261,33 @@ int hc_drift_select(const void* h_cached, const void* h_fresh, int32_t dtype, in
                     int32_t n_tokens, int32_t hidden, int64_t token_stride, int64_t seq_stride,
                     int32_t k, float* drift, int32_t* selected, void* stream);
 
+/* Block digests for cache lookup (host functions: every pointer is a host
+ * pointer; nothing runs on the GPU).  Two deterministic 128-bit BLAKE2b
+ * digests per block of block_size tokens, keyed by a per-tenant secret
+ * derived with HMAC-SHA256, with a public namespace for shared prefixes.
+ * [HyperCache page, "Core Design", item 1 "Dual-Mode Block Hashing".]
+ *
+ * hc_tenant_key: key_out[0..32) = HMAC-SHA256(master, "hc-tenant:" || tenant),
+ *   or HMAC-SHA256(master, "hc-public") when tenant is NULL or "" (the public
+ *   namespace).  master_len >= 0; tenant at most 4096 bytes. */
+int hc_tenant_key(const uint8_t* master, int32_t master_len, const char* tenant,
+                  uint8_t* key_out);
+
+/* hc_block_digests: blocks j < ceil(n_tokens / block_size) of `tokens`
+ * (block j = tokens [j*block_size, (j+1)*block_size), the last one may be
+ * short), each token as 4 little-endian bytes:
+ *   content_digests[j] = BLAKE2b-128(key; tokens of block j)
+ *   prefix_digests[j]  = BLAKE2b-128(key; prefix_digests[j-1] || tokens of block j)
+ * (prefix_digests[-1] is empty, so block 0's two digests are equal).  The
+ * content digest names a chunk wherever it sits (reuse at a new offset with
+ * the relative rotation); the prefix digest names it with everything before
+ * it (exact causal reuse).  key_len 1..64 (a tenant key is 32 bytes); the
+ * outputs hold 16 bytes per block.  BLAKE2b per RFC 7693, SHA-256 per
+ * FIPS 180-4, HMAC per RFC 2104. */
+int hc_block_digests(const int32_t* tokens, int64_t n_tokens, int32_t block_size,
+                     const uint8_t* key, int32_t key_len, uint8_t* prefix_digests,
+                     uint8_t* content_digests);
+
 /* Human-readable name of an hc_status value (static string, never NULL). */
 const char* hc_status_string(int32_t status);
 

@@ -20,7 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhc.so")
 
 SOURCES = ["api.cu", "encode.cu", "encode_rows.cu", "fetch_fp8.cu", "fetch_fp8_rows.cu",
-           "fetch_int4.cu", "fetch_raw.cu", "table.cu", "crc32.cu", "select.cu"]
+           "fetch_int4.cu", "fetch_raw.cu", "table.cu", "crc32.cu", "select.cu",
+           "hash.cpp"]
 HEADERS = [os.path.join(CSRC, h) for h in ("hc_internal.cuh", "fetch_impl.cuh", "encode_common.cuh",
                                             "fastdiv.h")] + [
     os.path.join(INCLUDE, "hc.h")]

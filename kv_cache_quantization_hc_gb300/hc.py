@@ -58,8 +58,11 @@ def lib():
         _I64 = ctypes.c_int64
         L.hc_crc32.argtypes = [_P, _I64, _I64, _P, _I64, _I64, _I32, _P, _P]
         L.hc_drift_select.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I64, _I64, _I32, _P, _P, _P]
+        L.hc_tenant_key.argtypes = [_P, _I32, ctypes.c_char_p, _P]
+        L.hc_block_digests.argtypes = [_P, _I64, _I32, _P, _I32, _P, _P]
         for fn in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
-                   "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select"):
+                   "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select", "hc_tenant_key",
+                   "hc_block_digests"):
             getattr(L, fn).restype = ctypes.c_int
         L.hc_status_string.argtypes = [_I32]
         L.hc_status_string.restype = ctypes.c_char_p
@@ -175,6 +178,29 @@ def drift_select(h_cached, h_fresh, k, drift=None, selected=None, stream=None):
     hc_drift_select(h_cached, h_fresh, dtype, n_seq, n_tokens, hidden, h_cached.stride(1),
                     h_cached.stride(0), k, drift, selected, stream)
     return drift, selected
+
+
+def tenant_key(master, tenant=None):
+    """hc_tenant_key on host bytes; returns the 32-byte secret."""
+    m = bytes(master)
+    out = ctypes.create_string_buffer(32)
+    _check("hc_tenant_key", lib().hc_tenant_key(
+        m, len(m), None if tenant is None else tenant.encode(), out))
+    return out.raw
+
+
+def block_digests(tokens, block_size, key):
+    """hc_block_digests on a host int32 sequence; returns (prefix, content)
+    as numpy uint8 arrays [n_blocks, 16]."""
+    import numpy as np
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    k = bytes(key)
+    n_blocks = -(-len(t) // block_size)
+    prefix = np.zeros((n_blocks, 16), np.uint8)
+    content = np.zeros((n_blocks, 16), np.uint8)
+    _check("hc_block_digests", lib().hc_block_digests(
+        t.ctypes.data, len(t), block_size, k, len(k), prefix.ctypes.data, content.ctypes.data))
+    return prefix, content
 
 
 def hc_build_delta_sincos(delta_m, n_distinct, d_head, rope_base, inv_freq, table, stream=None):

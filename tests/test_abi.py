@@ -30,7 +30,8 @@ def lib():
 def test_header_declares_the_calls():
     names = _declared_functions()
     for n in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
-              "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select", "hc_status_string"):
+              "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select", "hc_tenant_key",
+              "hc_block_digests", "hc_status_string"):
         assert n in names, names
 
 
