@@ -152,6 +152,28 @@ def test_fp8_rows_scale_overflow_encode(fmt):
     assert np.array_equal(g["scales"], o["scales"])
 
 
+# ---------------------------------------------------------------- extreme shapes
+@pytest.mark.parametrize("wire", ["fp8", "int4", "fp8_rows", "raw"])
+def test_many_heads_one_block(wire):
+    """32 KV heads, 128-token blocks, a single block whose n_valid is 1: a
+    unit of 8 sub-slabs is one head's slab, and all but one row is padding."""
+    c = parity.random_case(71, L=1, H=32, d=64, B=128, nb=1, src_fmt="bf16", out_fmt="bf16",
+                           pairing="interleaved")
+    c.n_valid = np.array([1], dtype=np.int32)
+    if wire == "raw":
+        c.src_k, c.src_v = parity.round_to(c.src_k, "bf16"), parity.round_to(c.src_v, "bf16")
+    _assert_ok(parity.run_case(c, wire))
+
+
+@pytest.mark.parametrize("wire", ["fp8", "int4", "fp8_rows"])
+def test_one_head_many_blocks(wire):
+    """One KV head: a unit of 8 sub-slabs spans four blocks (two slabs each),
+    with ragged tails and a mix of delta-m values."""
+    c = parity.random_case(72, L=3, H=1, d=128, B=16, nb=53, src_fmt="f16", out_fmt="f16",
+                           pairing="half_split", ragged=True, extra_slots=11)
+    _assert_ok(parity.run_case(c, wire))
+
+
 # ---------------------------------------------------------------- error paths
 def _tiny_path(wire="fp8", **over):
     from kv_cache_quantization_hc_gb300 import path as kvpath

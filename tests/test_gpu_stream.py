@@ -17,7 +17,7 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("wire", ["fp8", "int4"])
+@pytest.mark.parametrize("wire", ["fp8", "int4", "fp8_rows"])
 def test_layer_stream_matches_oracle(wire):
     from kv_cache_quantization_hc_gb300.path import KVPath
     from kv_cache_quantization_hc_gb300.stream import LayerStream
