@@ -17,8 +17,9 @@ __device__ __forceinline__ uint32_t fp8x2(float2 v) {
 // r = fp32(1/s) correctly rounded (Markstein, IBM J. Res. Dev. 34(1), 1990),
 // then one RNE-satfinite conversion.  q equals fp32(x / s) for every pair of
 // fp16 values and every pair of bf16 values (x, amax) with |x| <= amax and
-// s = fp32(amax / 448) >= 2^-90: the library's encoder is checked on all
-// 16-bit pairs against IEEE arithmetic (tests/test_gpu_exhaustive16.py).
+// s = fp32(amax / 448) >= 2^-90, or s that value rounded to fp16 (the
+// row-scaled wire): the library's encoders are checked on all 16-bit pairs
+// against IEEE arithmetic (tests/test_gpu_exhaustive16.py).
 // Exact E4M3 ties (x = 3/4 amax gives q = 336) therefore need no special
 // step.  The corrected quotient of -0 is +0, so the sign bits of the inputs
 // are OR-ed into the codes (for any other input the sign is already there).
