@@ -264,7 +264,7 @@ def run_ours(args):
     traffic = profiled_traffic(kname, "qwen3_8b") if not args.layers else None
     achieved = kern[dominant]["gbs"]
 
-    crc = run_crc(args, p, device) if args.crc else None
+    crc = run_crc(args, p, device, src_k, src_v) if args.crc else None
     e2e = None
     if "e2e" in args.legs:
         e2e = run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device,
@@ -311,9 +311,11 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_crc(args, p, device):
+def run_crc(args, p, device, src_k, src_v):
     """CRC-32 of the step's wire (one unit per (layer, block): its codes, then
-    its scales), timed alone with CUDA events after the step's own timing."""
+    its scales), timed alone with CUDA events after the step's own timing.
+    For the FP8 wire, also the encode with the fused per-slab CRC
+    (hc_encode_fp8_crc) against the plain encode."""
     import torch
     stream = torch.cuda.current_stream(device)
     out = torch.empty(p.L * p.nb, dtype=torch.int32, device=device)
@@ -329,9 +331,29 @@ def run_crc(args, p, device):
     torch.cuda.synchronize(device)
     avg = statistics.mean(a.elapsed_time(b) / 1e3 for a, b in evs)
     peak, _ = measured_peaks()
-    return {"kernel": "k_crc32", "units": p.L * p.nb, "bytes_per_launch": nbytes, "launches": reps,
-            "avg_ms": avg * 1e3, "gbs": nbytes / avg / 1e9, "frac": nbytes / avg / 1e9 / peak,
-            "bound": "hbm (read only)"}
+    out_d = {"kernel": "k_crc32", "units": p.L * p.nb, "bytes_per_launch": nbytes, "launches": reps,
+             "avg_ms": avg * 1e3, "gbs": nbytes / avg / 1e9, "frac": nbytes / avg / 1e9 / peak,
+             "bound": "shared-memory table lookups (the traffic is read-only HBM)"}
+    if args.codec == "fp8":
+        slab_crc = torch.empty((p.L, p.nb, 2, p.H), dtype=torch.int32, device=device)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            for a, b in ev:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize(device)
+            return statistics.mean(a.elapsed_time(b) / 1e3 for a, b in ev)
+        plain = timed(lambda: p.encode(src_k, src_v, stream=stream))
+        fused = timed(lambda: p.encode(src_k, src_v, stream=stream, crc=slab_crc))
+        out_d["fused_encode"] = {"kernel": "k_encode (fused slab CRC)", "units": slab_crc.numel(),
+                                 "encode_ms": plain * 1e3, "encode_with_crc_ms": fused * 1e3,
+                                 "separate_crc_ms": avg * 1e3}
+    return out_d
 
 
 def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device, device_step_s=None):

@@ -124,6 +124,22 @@ int hc_encode_fp8(const void* paged_k, const void* paged_v, const hc_paged_desc*
                   const int32_t* src_slots, const int32_t* n_valid, int32_t n_blocks,
                   uint8_t* codes, float* scales, int32_t* err_flag, void* stream);
 
+/* hc_encode_fp8_crc: hc_encode_fp8, and in the same pass the CRC-32 of every
+ * slab: crc[((l*n_blocks + j)*2 + kv)*n_kv_heads + h] = the CRC-32 (as
+ * hc_crc32 defines it) of the slab's block_size*d_head code bytes followed by
+ * the 4 bytes of its fp32 scale - hc_crc32(codes, B*d, B*d, scales, 4, 4,
+ * n_slabs).  For fp16/bf16 sources the CRC is folded into the encode as the
+ * codes are produced; for fp32 sources the call runs the CRC kernel after the
+ * encode.  Slabs of skipped blocks get no CRC.
+ * [HyperCache page, "Example output" part B: blocks stored with CRC32.]
+ *
+ *   crc : device u32 [n_layers][n_blocks][2][n_kv_heads], 4-byte aligned
+ * Other arguments as for hc_encode_fp8. */
+int hc_encode_fp8_crc(const void* paged_k, const void* paged_v, const hc_paged_desc* desc,
+                      const int32_t* src_slots, const int32_t* n_valid, int32_t n_blocks,
+                      uint8_t* codes, float* scales, uint32_t* crc, int32_t* err_flag,
+                      void* stream);
+
 /* hc_encode_int4: as hc_encode_fp8, but symmetric INT4 with one scale per
  * (layer, block, kv, head, token, group of `group` consecutive channels):
  *   s32 = fp32(amax / 7);  s = fp16_rne(s32) if scale_dtype == HC_F16, else s32;

@@ -75,6 +75,7 @@ hc::EncodeParams encode_params(const void* k, const void* v, const hc_paged_desc
   p.codes = codes;
   p.scales = scales;
   p.err = err;
+  p.crc = nullptr;
   return p;
 }
 
@@ -98,6 +99,37 @@ int hc_encode_fp8(const void* paged_k, const void* paged_v, const hc_paged_desc*
                                            codes, scales, err_flag, 0);
   return record(hc::launch_encode_fp8(desc->dtype, desc->d_head, p,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+int hc_encode_fp8_crc(const void* paged_k, const void* paged_v, const hc_paged_desc* desc,
+                      const int32_t* src_slots, const int32_t* n_valid, int32_t n_blocks,
+                      uint8_t* codes, float* scales, uint32_t* crc, int32_t* err_flag,
+                      void* stream) {
+  if (!crc || !aligned(crc, 4)) return HC_ERR_INVALID_ARG;
+  int st = check_paged(desc, paged_k, paged_v);
+  if (st != HC_OK) return st;
+  if (n_blocks < 0) return HC_ERR_INVALID_ARG;
+  if (!src_slots || !codes || !scales || !err_flag) return HC_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(scales, 4) || !aligned(err_flag, 4) ||
+      !aligned(src_slots, 4) || (n_valid && !aligned(n_valid, 4)))
+    return HC_ERR_INVALID_ARG;
+  if (!grid_fits(desc, n_blocks)) return HC_ERR_INVALID_ARG;
+  if (n_blocks == 0) return HC_OK;
+  hc::EncodeParams p = encode_params(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes,
+                                     scales, err_flag, 0);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (desc->dtype == HC_F32) {
+    // fp32 sources: the encode, then the CRC kernel over the same slab units
+    st = record(hc::launch_encode_fp8(desc->dtype, desc->d_head, p, s));
+    if (st != HC_OK) return st;
+    const int64_t slab = int64_t{desc->block_size} * desc->d_head;
+    return hc_crc32(codes, slab, slab, scales, 4, 4,
+                    static_cast<int32_t>(int64_t{desc->n_layers} * n_blocks * 2 * desc->n_kv_heads),
+                    crc, stream);
+  }
+  p.crc = crc;
+  hc::make_slab_crc_constants(desc->d_head, desc->block_size, &p);
+  return record(hc::launch_encode_fp8_crc(desc->dtype, desc->d_head, p, s));
 }
 
 int hc_encode_int4(const void* paged_k, const void* paged_v, const hc_paged_desc* desc,

@@ -22,38 +22,15 @@
 // 57(11), 2008): table k maps a byte to its register contribution when k
 // zero bytes follow it.  The 16 tables (16 KiB) are built in shared memory by
 // each CTA.
+#include "crc_math.h"
 #include "hc_internal.cuh"
 
 namespace hc {
 namespace {
 
-constexpr uint32_t kPolyReflected = 0xEDB88320u;
+constexpr uint32_t kPolyReflected = kCrcPolyReflected;
 constexpr int kTables = 16;
-
-__host__ __device__ inline uint32_t times_x(uint32_t v) {
-  return (v >> 1) ^ ((v & 1u) ? kPolyReflected : 0u);
-}
-
-// a * b mod P.
-__host__ __device__ inline uint32_t gf2_mul(uint32_t a, uint32_t b) {
-  uint32_t p = 0;
-  for (int i = 0; i < 32; ++i) {
-    if ((a >> (31 - i)) & 1u) p ^= b;
-    b = times_x(b);
-  }
-  return p;
-}
-
-// x^(8n) mod P.
-inline uint32_t x_pow_bytes(uint64_t n) {
-  uint32_t result = 0x80000000u;  // 1
-  uint32_t base = 0x40000000u;    // x
-  for (uint64_t e = 8 * n; e; e >>= 1) {
-    if (e & 1) result = gf2_mul(result, base);
-    base = gf2_mul(base, base);
-  }
-  return result;
-}
+inline uint32_t x_pow_bytes(uint64_t n) { return crc_x_pow_bytes(n); }
 
 // One 16-byte word (bytes in memory order) into register r.
 __device__ __forceinline__ uint32_t step16(const uint32_t (*T)[256], uint32_t r, uint4 w) {

@@ -53,7 +53,9 @@
 // Reads use the streaming cache hint (each element is read once); codes are
 // written with streaming stores.
 #include <algorithm>
+#include <type_traits>
 
+#include "crc_math.h"
 #include "encode_common.cuh"
 
 namespace hc {
@@ -267,10 +269,61 @@ __device__ __forceinline__ void load_rows(const EncodeParams& p, const Where& w,
   }
 }
 
-template <typename SrcT, int D>
+// ---------------------------------------------------------------- Fused CRC
+// The FP8 encoder can also write the CRC-32/ISO-HDLC of every slab - its
+// B x d code bytes, then its 4-byte fp32 scale - the unit hc_crc32 computes
+// for a = codes (B d bytes apart), b = scales (4 bytes apart).  CRCs are
+// linear over GF(2) (see crc_math.h), so each lane folds its own code words
+// as it produces them: a lane's pieces (8 bytes per pass) lie 256 bytes
+// apart, so its register moves to the next piece's end by a multiplication
+// with K = x^(8*256), done with four byte tables built from crc_kbasis, and
+// takes in the piece's own CRC by slicing-by-8.  After the last pass, one
+// multiplication moves it to the end of the sub-slab (crc_lane), the warp
+// xor-reduces, the sub-slabs of a slab combine in shared memory (crc_sub),
+// and the scale bytes, the initial register and the final xor are added.
+struct CrcTables {
+  uint32_t t[8][256];  // t[k][v]: register contribution of byte v followed by k zero bytes
+  uint32_t m[4][256];  // m[b][v]: (v << 8b) * K mod P
+};
+
+__device__ __forceinline__ void build_crc_tables(const EncodeParams& p, CrcTables& tab) {
+  for (int v = threadIdx.x; v < 256; v += kThreads) {
+    uint32_t c = v;
+    for (int i = 0; i < 8; ++i) c = crc_times_x(c);
+    tab.t[0][v] = c;
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < 256; v += kThreads) {
+    uint32_t c = tab.t[0][v];
+    for (int k = 1; k < 8; ++k) {
+      c = (c >> 8) ^ tab.t[0][c & 0xff];
+      tab.t[k][v] = c;
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t m = 0;
+      for (int j = 0; j < 8; ++j)
+        if ((v >> j) & 1) m ^= p.crc_kbasis[8 * b + j];
+      tab.m[b][v] = m;
+    }
+  }
+  __syncthreads();
+}
+
+// acc * K + CRC(8 code bytes c), register started at 0.
+__device__ __forceinline__ uint32_t crc_fold(const CrcTables& tab, uint32_t acc, uint2 c) {
+  const uint32_t mk = tab.m[0][acc & 0xff] ^ tab.m[1][(acc >> 8) & 0xff] ^
+                      tab.m[2][(acc >> 16) & 0xff] ^ tab.m[3][acc >> 24];
+  return mk ^ tab.t[7][c.x & 0xff] ^ tab.t[6][(c.x >> 8) & 0xff] ^ tab.t[5][(c.x >> 16) & 0xff] ^
+         tab.t[4][c.x >> 24] ^ tab.t[3][c.y & 0xff] ^ tab.t[2][(c.y >> 8) & 0xff] ^
+         tab.t[1][(c.y >> 16) & 0xff] ^ tab.t[0][c.y >> 24];
+}
+
+template <typename SrcT, int D, bool kCrc>
 __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where& w,
                                              const SlotInfo& si, int chunk, int rr, int warp,
-                                             int lane, float* s_amax,
+                                             int lane, float* s_amax, uint32_t* s_crc,
+                                             const CrcTables* tab,
                                              const Raw8<SrcT> (&raw)[EncodeGeom<D>::kPasses]) {
   using G = EncodeGeom<D>;
   const int bad = w.active ? slot_errors(p, si) : 0;
@@ -290,7 +343,12 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
     for (int k = 0; k < wps; ++k) amax = fmaxf(amax, s_amax[first + k]);
   }
   if (bad && lane == 0) flag_error(p.err, bad);
-  if (!ok) return;
+  if (!ok) {
+    if constexpr (kCrc) {
+      if (wps > 1) __syncthreads();  // the slab combine below; uniform over the CTA
+    }
+    return;
+  }
 
   const float s = __fdiv_rn(amax, 448.0f);
   uint8_t* out = p.codes + w.slab * static_cast<int64_t>(p.B) * D + chunk * 8;
@@ -301,15 +359,44 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
     // about 2^-81) and s = 0 take the IEEE division.
     uint2* dst = reinterpret_cast<uint2*>(out + static_cast<int64_t>(row0) * D);
     constexpr int kPassStride = G::kRowsPerPass * D / 8;  // in uint2
+    uint32_t acc = 0;  // fused CRC: this lane's pieces so far
     if (s >= 0x1p-90f) {
       const float r = __frcp_rn(s);
 #pragma unroll
-      for (int i = 0; i < G::kPasses; ++i) __stcs(dst + i * kPassStride, fp8x8_corrected(raw[i], s, r));
+      for (int i = 0; i < G::kPasses; ++i) {
+        const uint2 c = fp8x8_corrected(raw[i], s, r);
+        __stcs(dst + i * kPassStride, c);
+        if constexpr (kCrc) acc = crc_fold(*tab, acc, c);
+      }
     } else {
 #pragma unroll
-      for (int i = 0; i < G::kPasses; ++i) __stcs(dst + i * kPassStride, fp8x8_divide(raw[i], s));
+      for (int i = 0; i < G::kPasses; ++i) {
+        const uint2 c = fp8x8_divide(raw[i], s);
+        __stcs(dst + i * kPassStride, c);
+        if constexpr (kCrc) acc = crc_fold(*tab, acc, c);
+      }
     }
     if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
+    if constexpr (kCrc) {
+      acc = gf2_mul(acc, p.crc_lane[lane]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+      if (wps > 1) {
+        if (lane == 0) s_crc[warp] = acc;
+        __syncthreads();
+        if (w.sub == 0) {
+          const int first = warp;
+          acc = 0;
+          for (int k = 0; k < wps; ++k) acc ^= gf2_mul(s_crc[first + k], p.crc_sub[k]);
+        }
+      }
+      if (w.sub == 0 && lane == 0) {
+        const uint32_t sb = __float_as_uint(s);  // the scale's 4 bytes, little-endian
+        const uint32_t scale_crc = tab->t[3][sb & 0xff] ^ tab->t[2][(sb >> 8) & 0xff] ^
+                                   tab->t[1][(sb >> 16) & 0xff] ^ tab->t[0][sb >> 24];
+        p.crc[w.slab] = gf2_mul(acc, p.crc_tail) ^ scale_crc ^ p.crc_init;
+      }
+    }
     return;
   }
   // fp32 sources: the bracketed products with the deferred exact tie step.
@@ -546,11 +633,21 @@ __global__ void __launch_bounds__(kThreads, HC_ENCODE_WIDE_MIN_BLOCKS) k_encode_
 // launch for FP8 with larger blocks (whose units meet at a CTA barrier) and
 // for INT4.
 // kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
-template <typename SrcT, int D, int kWire, bool kFlat, int kGroupLog2>
+// kCrc: the FP8 wire with the fused slab CRC (16-bit sources).
+template <typename SrcT, int D, int kWire, bool kFlat, int kGroupLog2, bool kCrc = false>
 __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams p) {
   using G = EncodeGeom<D>;
   constexpr bool kDoubleBuffer = !kFlat && sizeof(SrcT) == 2;
+  static_assert(!kCrc || (kWire == 0 && sizeof(SrcT) == 2), "fused CRC: FP8, 16-bit sources");
   __shared__ float s_amax[2][kWarps];
+  __shared__ uint32_t s_crc[2][kWarps];
+  using Tab = typename std::conditional<kCrc, CrcTables, char>::type;
+  __shared__ Tab crc_tab;
+  const CrcTables* tab = nullptr;
+  if constexpr (kCrc) {
+    build_crc_tables(p, crc_tab);
+    tab = &crc_tab;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = lane % G::kChunksPerRow, rr = lane / G::kChunksPerRow;
   const uint32_t stride = gridDim.x;
@@ -560,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
   auto process = [&](const Where& w, const SlotInfo& si, const Raw8<SrcT>(&raw)[G::kPasses],
                      int parity) {
     if constexpr (kWire == 0)
-      quantize_fp8<SrcT, D>(p, w, si, chunk, rr, warp, lane, s_amax[parity], raw);
+      quantize_fp8<SrcT, D, kCrc>(p, w, si, chunk, rr, warp, lane, s_amax[parity], s_crc[parity], tab,
+                                  raw);
     else
       quantize_int4<SrcT, D, kWire == 1, kGroupLog2>(p, w, si, chunk, rr, lane, raw);
   };
@@ -658,6 +756,46 @@ cudaError_t encode_dispatch(int dtype, int d, const EncodeParams& p, cudaStream_
 
 cudaError_t launch_encode_fp8(int dtype, int d, const EncodeParams& p, cudaStream_t s) {
   return encode_dispatch<0>(dtype, d, p, s);
+}
+
+void make_slab_crc_constants(int d, int block_size, EncodeParams* p) {
+  const uint32_t k = crc_x_pow_bytes(256);
+  for (int j = 0; j < 32; ++j) p->crc_kbasis[j] = gf2_mul(1u << j, k);
+  const int chunks_per_row = d / 8, rows_per_pass = 32 / chunks_per_row;
+  const int passes = kRowsPerWarp / rows_per_pass;
+  for (int lane = 0; lane < 32; ++lane) {
+    const int chunk = lane % chunks_per_row, rr = lane / chunks_per_row;
+    const int last_end = rr * d + chunk * 8 + (passes - 1) * rows_per_pass * d + 8;
+    p->crc_lane[lane] = crc_x_pow_bytes(static_cast<uint64_t>(kRowsPerWarp * d - last_end));
+  }
+  const int64_t slab = static_cast<int64_t>(block_size) * d;
+  for (int sub = 0; sub < 8; ++sub) {
+    const int64_t after = slab - static_cast<int64_t>(kRowsPerWarp) * d * (sub + 1);
+    p->crc_sub[sub] = after >= 0 ? crc_x_pow_bytes(static_cast<uint64_t>(after)) : 0u;
+  }
+  p->crc_tail = crc_x_pow_bytes(4);
+  p->crc_init = gf2_mul(0xFFFFFFFFu, crc_x_pow_bytes(static_cast<uint64_t>(slab + 4))) ^ 0xFFFFFFFFu;
+}
+
+template <typename SrcT, int D>
+cudaError_t encode_crc_t(const EncodeParams& p, cudaStream_t s) {
+  if (p.B > kRowsPerWarp) {
+    k_encode<SrcT, D, 0, true, 0, true><<<p.grid.units, kThreads, 0, s>>>(p);
+  } else {
+    const uint32_t grid = static_cast<uint32_t>(
+        std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * 2));
+    k_encode<SrcT, D, 0, false, 0, true><<<grid, kThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_fp8_crc(int dtype, int d, const EncodeParams& p, cudaStream_t s) {
+  switch (dtype) {
+    case HC_F16: return d == 64 ? encode_crc_t<__half, 64>(p, s) : encode_crc_t<__half, 128>(p, s);
+    case HC_BF16:
+      return d == 64 ? encode_crc_t<__nv_bfloat16, 64>(p, s) : encode_crc_t<__nv_bfloat16, 128>(p, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_encode_int4(int dtype, int d, bool scale_f16, const EncodeParams& p,

@@ -61,6 +61,15 @@ struct EncodeParams {
   uint8_t* codes;
   void* scales;
   int32_t* err;
+  // CRC-32 of every FP8 slab (its B x d codes, then its 4-byte scale), fused
+  // into the encode when crc != null; the constants are built on the host
+  // (see encode.cu, "Fused CRC").
+  uint32_t* crc;
+  uint32_t crc_kbasis[32];  // x^(8*256) times each single-bit register value
+  uint32_t crc_lane[32];    // x^(8 * bytes from a lane's last piece to its sub-slab's end)
+  uint32_t crc_sub[8];      // x^(8 * bytes from sub-slab k's end to the slab's codes' end)
+  uint32_t crc_tail;        // x^(8*4): past the scale bytes
+  uint32_t crc_init;        // the initial register's term and the final xor
 };
 
 struct FetchParams {
@@ -116,6 +125,10 @@ struct SelectParams {
 
 // Launchers: return the launch's cudaError_t.  `dtype`/`out_dtype` are hc_dtype.
 cudaError_t launch_encode_fp8(int dtype, int d, const EncodeParams& p, cudaStream_t s);
+// The FP8 encode with the fused slab CRC (16-bit sources; p.crc != null and
+// the constants filled by make_slab_crc_constants).
+cudaError_t launch_encode_fp8_crc(int dtype, int d, const EncodeParams& p, cudaStream_t s);
+void make_slab_crc_constants(int d, int block_size, EncodeParams* p);
 cudaError_t launch_encode_fp8_rows(int dtype, int d, bool scale_f16, const EncodeParams& p,
                                    cudaStream_t s);
 cudaError_t launch_fetch_fp8_rows(int out_dtype, int d, bool half_split, bool scale_f16,

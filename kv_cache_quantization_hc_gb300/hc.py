@@ -52,6 +52,7 @@ def lib():
         L.hc_encode_fp8.argtypes = [_P, _P, desc_p, _P, _P, _I32, _P, _P, _P, _P]
         L.hc_encode_int4.argtypes = [_P, _P, desc_p, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]
         L.hc_encode_fp8_rows.argtypes = [_P, _P, desc_p, _P, _P, _I32, _I32, _P, _P, _P, _P]
+        L.hc_encode_fp8_crc.argtypes = [_P, _P, desc_p, _P, _P, _I32, _P, _P, _P, _P, _P]
         L.hc_build_delta_sincos.argtypes = [_P, _I32, _I32, ctypes.c_double, _P, _P, _P]
         L.hc_fetch_rotate_scatter.argtypes = [_I32, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _P, _P,
                                               _I32, _P, _P, desc_p, _P, _P]
@@ -60,7 +61,8 @@ def lib():
         L.hc_drift_select.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I64, _I64, _I32, _P, _P, _P]
         L.hc_tenant_key.argtypes = [_P, _I32, ctypes.c_char_p, _P]
         L.hc_block_digests.argtypes = [_P, _I64, _I32, _P, _I32, _P, _P]
-        for fn in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
+        for fn in ("hc_encode_fp8", "hc_encode_fp8_crc", "hc_encode_int4", "hc_encode_fp8_rows",
+                   "hc_build_delta_sincos",
                    "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select", "hc_tenant_key",
                    "hc_block_digests"):
             getattr(L, fn).restype = ctypes.c_int
@@ -130,6 +132,13 @@ def hc_encode_fp8(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes, s
     _check("hc_encode_fp8", lib().hc_encode_fp8(
         _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
         n_blocks, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
+
+
+def hc_encode_fp8_crc(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes, scales, crc,
+                      err_flag, stream=None):
+    _check("hc_encode_fp8_crc", lib().hc_encode_fp8_crc(
+        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
+        n_blocks, _ptr(codes), _ptr(scales), _ptr(crc), _ptr(err_flag), _stream(stream)))
 
 
 def hc_encode_int4(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, group, scale_dtype,

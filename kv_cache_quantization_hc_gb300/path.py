@@ -55,11 +55,18 @@ class KVPath:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
 
     # -- steps ----------------------------------------------------------------
-    def encode(self, src_k, src_v, desc=None, stream=None, codes=None, scales=None):
+    def encode(self, src_k, src_v, desc=None, stream=None, codes=None, scales=None, crc=None):
+        """Encode; with `crc` (device int32/uint32 [L, NB, 2, H], FP8 wire only)
+        the same pass writes each slab's CRC-32 (its codes, then its scale)."""
         desc = desc or hc.paged_desc(src_k)
         codes = self.codes if codes is None else codes
         scales = self.scales if scales is None else scales
-        if self.wire == hc.HC_WIRE_FP8:
+        if crc is not None and self.wire != hc.HC_WIRE_FP8:
+            raise ValueError("the fused CRC is built for the FP8 wire")
+        if self.wire == hc.HC_WIRE_FP8 and crc is not None:
+            hc.hc_encode_fp8_crc(src_k, src_v, desc, self.src_slots, self.n_valid, self.nb,
+                                 codes, scales, crc, self.err, stream)
+        elif self.wire == hc.HC_WIRE_FP8:
             hc.hc_encode_fp8(src_k, src_v, desc, self.src_slots, self.n_valid, self.nb,
                              codes, scales, self.err, stream)
         elif self.wire == hc.HC_WIRE_INT4:

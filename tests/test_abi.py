@@ -29,7 +29,8 @@ def lib():
 
 def test_header_declares_the_calls():
     names = _declared_functions()
-    for n in ("hc_encode_fp8", "hc_encode_int4", "hc_encode_fp8_rows", "hc_build_delta_sincos",
+    for n in ("hc_encode_fp8", "hc_encode_fp8_crc", "hc_encode_int4", "hc_encode_fp8_rows",
+              "hc_build_delta_sincos",
               "hc_fetch_rotate_scatter", "hc_crc32", "hc_drift_select", "hc_tenant_key",
               "hc_block_digests", "hc_status_string"):
         assert n in names, names
@@ -128,3 +129,14 @@ def test_host_validation_of_drift_select(lib):
     assert d(A, A, hc.HC_BF16, 2, 100, 64, 64, 6000, 15, A, A, None) == hc.HC_ERR_INVALID_ARG   # overlap
     assert d(A + 8, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 15, A, A, None) == hc.HC_ERR_INVALID_ARG
     assert d(A, A, hc.HC_BF16, 0, 100, 64, 64, 6400, 15, A, A, None) == hc.HC_OK
+
+
+def test_host_validation_of_fused_crc(lib):
+    from kv_cache_quantization_hc_gb300 import hc
+    A = 1 << 20
+    good = hc.hc_paged_desc(1, 8, 128, 16, 4, hc.HC_BF16, 16 * 8 * 128, 0)
+    P = ctypes.byref
+    e = lib.hc_encode_fp8_crc
+    assert e(A, A, P(good), A, None, 1, A, A, None, A, None) == hc.HC_ERR_INVALID_ARG     # no crc
+    assert e(A, A, P(good), A, None, 1, A, A, A + 2, A, None) == hc.HC_ERR_INVALID_ARG    # alignment
+    assert e(A, A, P(good), A, None, 0, A, A, A, A, None) == hc.HC_OK

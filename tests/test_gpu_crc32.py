@@ -85,3 +85,37 @@ def test_crc32_of_the_wire_and_tamper_detection(wire):
     got2 = _u32(p.crc32())
     changed = np.nonzero(got2 != got)[0]
     assert changed.tolist() == [u]
+
+
+FUSED = [  # d, B, src dtype, ragged, H
+    (128, 16, "bf16", True, 8), (128, 16, "f16", False, 3), (64, 16, "bf16", True, 2),
+    (128, 64, "bf16", True, 4), (64, 32, "f16", True, 3), (128, 128, "bf16", False, 2),
+    (128, 16, "f32", True, 3), (64, 64, "f32", False, 2)]
+
+
+@pytest.mark.parametrize("d,B,src,ragged,H", FUSED)
+def test_fused_slab_crc_matches_the_oracle(d, B, src, ragged, H):
+    """hc_encode_fp8_crc: every slab's CRC (its codes, then its fp32 scale)
+    equals the oracle's CRC of the oracle's wire for that slab."""
+    from kv_cache_quantization_hc_gb300 import path as kvpath
+    c = parity.random_case(81 + B + d, L=3, H=H, d=d, B=B, nb=9, src_fmt=src, out_fmt="bf16",
+                           ragged=ragged)
+    o = parity.oracle_run(c, "fp8")
+    dm_vals, dm_idx = np.unique(c.delta_m, return_inverse=True)
+    p = kvpath.KVPath(n_layers=c.L, H=c.H, d=c.d, B=c.B, n_blocks=len(c.src_slots),
+                      src_slots=c.src_slots, dst_slots=c.dst_slots, n_valid=c.n_valid,
+                      delta_m_distinct=dm_vals, delta_idx=dm_idx, wire="fp8", pairing=c.pairing,
+                      rope_base=c.rope_base, paged_dtype="bf16")
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[src]
+    src_k = torch.as_tensor(c.src_k, device=DEV).to(tdt)
+    src_v = torch.as_tensor(c.src_v, device=DEV).to(tdt)
+    crc = torch.zeros((c.L, len(c.src_slots), 2, c.H), dtype=torch.int32, device=DEV)
+    p.encode(src_k, src_v, crc=crc)
+    torch.cuda.synchronize()
+    assert p.error_bits() == 0
+    assert np.array_equal(p.codes.cpu().numpy(), o["codes"])
+    n = crc.numel()
+    codes = o["codes"].reshape(n, -1)
+    scales = o["scales"].astype(np.float32).reshape(n, 1).view(np.uint8)
+    want = ocrc.crc32_units(codes, codes.shape[1], codes.shape[1], n, scales, 4, 4)
+    assert np.array_equal(_u32(crc).reshape(-1), want)
