@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 METRIC = "KV fetch+rotate+scatter GB/s and tokens/s; % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {
-    "k_encode": ["encode.cu", "encode_common.cuh", "hc_internal.cuh", "fastdiv.h"],
+    "k_encode": ["encode.cu", "encode_common.cuh", "crc_math.h", "hc_internal.cuh", "fastdiv.h"],
     "k_fetch": ["fetch_impl.cuh", "fetch_fp8.cu", "hc_internal.cuh", "fastdiv.h"],
     "k_encode_fp8_rows": ["encode_rows.cu", "encode_common.cuh", "hc_internal.cuh", "fastdiv.h"],
     "k_fetch_fp8_rows": ["fetch_impl.cuh", "fetch_fp8_rows.cu", "hc_internal.cuh", "fastdiv.h"],

@@ -21,10 +21,12 @@
 // this write-heavy kernel gains more from resident warps than from software
 // pipelining.  The same code runs persistent CTAs that step through units
 // with a per-warp prefetch of the next unit when built with
-// HC_FETCH_CTAS_PER_SM / HC_FETCH_DOUBLE_BUFFER (see hc_internal.cuh).  Each store instruction writes 8 output elements per
-// lane; neighbouring lanes write neighbouring 16-byte pieces of one token
-// row, and the 8 warps of a unit write neighbouring heads.  Products are
-// formed two at a time (FMUL2 / FFMA2).
+// HC_FETCH_CTAS_PER_SM / HC_FETCH_DOUBLE_BUFFER (see hc_internal.cuh).
+// Each store instruction writes 8 output elements per lane; neighbouring
+// lanes write neighbouring 16-byte pieces of one token row, and the 8 warps
+// of a unit write neighbouring heads.  Stores are streaming (measured faster
+// than write-back stores here).  Products are formed two at a time
+// (FMUL2 / FFMA2).
 #pragma once
 
 #include <algorithm>
