@@ -412,14 +412,19 @@ def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device, dev
     if device_step_s:
         # each part alone: the whole source up, the whole result down
         def alone(fn):
+            # the best of three runs: a part's own time, free of interference
             fn()
             torch.cuda.synchronize(device)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            torch.cuda.synchronize(device)
-            return e0.elapsed_time(e1) / 1e3
+            best = None
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                t = e0.elapsed_time(e1) / 1e3
+                best = t if best is None else min(best, t)
+            return best
         up = alone(lambda: (src_k.copy_(h_src_k, non_blocking=True), src_v.copy_(h_src_v, non_blocking=True)))
         down = alone(lambda: (h_dst_k.copy_(dst_k, non_blocking=True), h_dst_v.copy_(dst_v, non_blocking=True)))
         serial = up + device_step_s + down
