@@ -277,13 +277,17 @@ __device__ __forceinline__ void load_rows(const EncodeParams& p, const Where& w,
 // as it produces them: a lane's pieces (8 bytes per pass) lie 256 bytes
 // apart, so its register moves to the next piece's end by a multiplication
 // with K = x^(8*256), done with four byte tables built from crc_kbasis, and
-// takes in the piece's own CRC by slicing-by-8.  After the last pass, one
-// multiplication moves it to the end of the sub-slab (crc_lane), the warp
-// xor-reduces, the sub-slabs of a slab combine in shared memory (crc_sub),
-// and the scale bytes, the initial register and the final xor are added.
+// takes in the piece's own CRC by slicing-by-8 (persistent CTAs instead build
+// position tables once, which do both in 8 lookups).  After the last pass a
+// butterfly over the lanes (crc_lane_tree) brings the warp's register to the
+// end of the sub-slab, the sub-slabs of a slab combine in shared memory
+// (crc_sub), and the scale bytes, the initial register and the final xor are
+// added.
 struct CrcTables {
-  uint32_t t[8][256];  // t[k][v]: register contribution of byte v followed by k zero bytes
-  uint32_t m[4][256];  // m[b][v]: (v << 8b) * K mod P
+  uint32_t t[8][256];       // t[k][v]: register contribution of byte v followed by k zero bytes
+  uint32_t m[4][256];       // m[b][v]: (v << 8b) * K mod P
+  uint32_t lvl[5][4][256];  // lvl[j][b][v]: (v << 8b) * x^(64 * 2^j) mod P (the lane tree)
+  uint32_t basis[5][32];    // x^(64 * 2^j) times each single-bit value
 };
 
 __device__ __forceinline__ void build_crc_tables(const EncodeParams& p, CrcTables& tab) {
@@ -292,7 +296,16 @@ __device__ __forceinline__ void build_crc_tables(const EncodeParams& p, CrcTable
     for (int i = 0; i < 8; ++i) c = crc_times_x(c);
     tab.t[0][v] = c;
   }
+  for (int e = threadIdx.x; e < 5 * 32; e += kThreads)
+    tab.basis[e / 32][e % 32] = gf2_mul(1u << (e % 32), p.crc_level[e / 32]);
   __syncthreads();
+  for (int e = threadIdx.x; e < 5 * 4 * 256; e += kThreads) {
+    const int j = e / 1024, b = (e / 256) % 4, v = e % 256;
+    uint32_t m = 0;
+    for (int q = 0; q < 8; ++q)
+      if ((v >> q) & 1) m ^= tab.basis[j][8 * b + q];
+    tab.lvl[j][b][v] = m;
+  }
   for (int v = threadIdx.x; v < 256; v += kThreads) {
     uint32_t c = tab.t[0][v];
     for (int k = 1; k < 8; ++k) {
@@ -310,6 +323,44 @@ __device__ __forceinline__ void build_crc_tables(const EncodeParams& p, CrcTable
   __syncthreads();
 }
 
+// Position tables (persistent launch): pos[i][k][v] is the contribution of
+// byte v at byte k of a lane's pass-i piece, moved to the end of the lane's
+// last piece - the byte table t[7-k] multiplied by K once per later pass.
+// With them a pass costs 8 lookups instead of 12 (no K step).
+template <int kPasses>
+__device__ __forceinline__ void build_crc_pos_tables(const CrcTables& tab, uint32_t* pos) {
+  for (int e = threadIdx.x; e < kPasses * 8 * 256; e += kThreads) {
+    const int i = e / 2048, k = (e / 256) % 8, v = e % 256;
+    uint32_t c = tab.t[7 - k][v];
+    for (int n = i; n < kPasses - 1; ++n)
+      c = tab.m[0][c & 0xff] ^ tab.m[1][(c >> 8) & 0xff] ^ tab.m[2][(c >> 16) & 0xff] ^ tab.m[3][c >> 24];
+    pos[e] = c;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t crc_pos(const uint32_t* pos_i, uint2 c) {
+  const uint32_t(*t)[256] = reinterpret_cast<const uint32_t(*)[256]>(pos_i);
+  return t[0][c.x & 0xff] ^ t[1][(c.x >> 8) & 0xff] ^ t[2][(c.x >> 16) & 0xff] ^ t[3][c.x >> 24] ^
+         t[4][c.y & 0xff] ^ t[5][(c.y >> 8) & 0xff] ^ t[6][(c.y >> 16) & 0xff] ^ t[7][c.y >> 24];
+}
+
+// The warp's register from each lane's (positioned at the end of the lane's
+// last piece; lane l's pieces start at byte 8l of each 256-byte pass block):
+// a butterfly in which the lower lane of each pair moves its value 8 * 2^j
+// bytes on (a table multiplication by x^(64 * 2^j)) and adds its partner's.
+// Lane 0 ends with the value at the end of the sub-slab.
+__device__ __forceinline__ uint32_t crc_lane_tree(const CrcTables& tab, uint32_t acc, int lane) {
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, acc, 1 << j);
+    const uint32_t moved = tab.lvl[j][0][acc & 0xff] ^ tab.lvl[j][1][(acc >> 8) & 0xff] ^
+                           tab.lvl[j][2][(acc >> 16) & 0xff] ^ tab.lvl[j][3][acc >> 24];
+    acc = ((lane >> j) & 1) ? acc : (moved ^ other);
+  }
+  return acc;
+}
+
 // acc * K + CRC(8 code bytes c), register started at 0.
 __device__ __forceinline__ uint32_t crc_fold(const CrcTables& tab, uint32_t acc, uint2 c) {
   const uint32_t mk = tab.m[0][acc & 0xff] ^ tab.m[1][(acc >> 8) & 0xff] ^
@@ -323,7 +374,7 @@ template <typename SrcT, int D, bool kCrc>
 __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where& w,
                                              const SlotInfo& si, int chunk, int rr, int warp,
                                              int lane, float* s_amax, uint32_t* s_crc,
-                                             const CrcTables* tab,
+                                             const CrcTables* tab, const uint32_t* pos,
                                              const Raw8<SrcT> (&raw)[EncodeGeom<D>::kPasses]) {
   using G = EncodeGeom<D>;
   const int bad = w.active ? slot_errors(p, si) : 0;
@@ -366,21 +417,19 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
       for (int i = 0; i < G::kPasses; ++i) {
         const uint2 c = fp8x8_corrected(raw[i], s, r);
         __stcs(dst + i * kPassStride, c);
-        if constexpr (kCrc) acc = crc_fold(*tab, acc, c);
+        if constexpr (kCrc) acc = pos ? acc ^ crc_pos(pos + i * 2048, c) : crc_fold(*tab, acc, c);
       }
     } else {
 #pragma unroll
       for (int i = 0; i < G::kPasses; ++i) {
         const uint2 c = fp8x8_divide(raw[i], s);
         __stcs(dst + i * kPassStride, c);
-        if constexpr (kCrc) acc = crc_fold(*tab, acc, c);
+        if constexpr (kCrc) acc = pos ? acc ^ crc_pos(pos + i * 2048, c) : crc_fold(*tab, acc, c);
       }
     }
     if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
     if constexpr (kCrc) {
-      acc = gf2_mul(acc, p.crc_lane[lane]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+      acc = crc_lane_tree(*tab, acc, lane);  // lane 0: the sub-slab's register
       if (wps > 1) {
         if (lane == 0) s_crc[warp] = acc;
         __syncthreads();
@@ -644,9 +693,15 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
   using Tab = typename std::conditional<kCrc, CrcTables, char>::type;
   __shared__ Tab crc_tab;
   const CrcTables* tab = nullptr;
+  const uint32_t* pos = nullptr;
   if constexpr (kCrc) {
     build_crc_tables(p, crc_tab);
     tab = &crc_tab;
+    if constexpr (!kFlat) {  // persistent CTAs build the position tables once
+      extern __shared__ uint32_t crc_pos_smem[];
+      build_crc_pos_tables<G::kPasses>(crc_tab, crc_pos_smem);
+      pos = crc_pos_smem;
+    }
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = lane % G::kChunksPerRow, rr = lane / G::kChunksPerRow;
@@ -658,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
                      int parity) {
     if constexpr (kWire == 0)
       quantize_fp8<SrcT, D, kCrc>(p, w, si, chunk, rr, warp, lane, s_amax[parity], s_crc[parity], tab,
-                                  raw);
+                                  pos, raw);
     else
       quantize_int4<SrcT, D, kWire == 1, kGroupLog2>(p, w, si, chunk, rr, lane, raw);
   };
@@ -761,13 +816,7 @@ cudaError_t launch_encode_fp8(int dtype, int d, const EncodeParams& p, cudaStrea
 void make_slab_crc_constants(int d, int block_size, EncodeParams* p) {
   const uint32_t k = crc_x_pow_bytes(256);
   for (int j = 0; j < 32; ++j) p->crc_kbasis[j] = gf2_mul(1u << j, k);
-  const int chunks_per_row = d / 8, rows_per_pass = 32 / chunks_per_row;
-  const int passes = kRowsPerWarp / rows_per_pass;
-  for (int lane = 0; lane < 32; ++lane) {
-    const int chunk = lane % chunks_per_row, rr = lane / chunks_per_row;
-    const int last_end = rr * d + chunk * 8 + (passes - 1) * rows_per_pass * d + 8;
-    p->crc_lane[lane] = crc_x_pow_bytes(static_cast<uint64_t>(kRowsPerWarp * d - last_end));
-  }
+  for (int j = 0; j < 5; ++j) p->crc_level[j] = crc_x_pow_bytes(8u << j);
   const int64_t slab = static_cast<int64_t>(block_size) * d;
   for (int sub = 0; sub < 8; ++sub) {
     const int64_t after = slab - static_cast<int64_t>(kRowsPerWarp) * d * (sub + 1);
@@ -782,9 +831,14 @@ cudaError_t encode_crc_t(const EncodeParams& p, cudaStream_t s) {
   if (p.B > kRowsPerWarp) {
     k_encode<SrcT, D, 0, true, 0, true><<<p.grid.units, kThreads, 0, s>>>(p);
   } else {
+    constexpr int kPosBytes = EncodeGeom<D>::kPasses * 8 * 256 * 4;
+    auto kern = k_encode<SrcT, D, 0, false, 0, true>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPosBytes);
+    if (e != cudaSuccess) return e;
     const uint32_t grid = static_cast<uint32_t>(
         std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * 2));
-    k_encode<SrcT, D, 0, false, 0, true><<<grid, kThreads, 0, s>>>(p);
+    kern<<<grid, kThreads, kPosBytes, s>>>(p);
   }
   return cudaGetLastError();
 }

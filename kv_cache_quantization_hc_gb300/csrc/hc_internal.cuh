@@ -66,7 +66,7 @@ struct EncodeParams {
   // (see encode.cu, "Fused CRC").
   uint32_t* crc;
   uint32_t crc_kbasis[32];  // x^(8*256) times each single-bit register value
-  uint32_t crc_lane[32];    // x^(8 * bytes from a lane's last piece to its sub-slab's end)
+  uint32_t crc_level[5];    // x^(64 * 2^j): the lanes' butterfly steps
   uint32_t crc_sub[8];      // x^(8 * bytes from sub-slab k's end to the slab's codes' end)
   uint32_t crc_tail;        // x^(8*4): past the scale bytes
   uint32_t crc_init;        // the initial register's term and the final xor
