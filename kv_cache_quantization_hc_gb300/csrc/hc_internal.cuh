@@ -170,10 +170,6 @@ inline int device_sm_count() {
   return 152;
 }
 
-// Grid for a kernel with one warp per 16-row sub-slab.
-__host__ __device__ inline int64_t sub_slab_count(int64_t n_layers, int64_t n_blocks, int64_t H, int64_t B) {
-  return n_layers * n_blocks * 2 * H * (B / kRowsPerWarp);
-}
 
 // ---------------------------------------------------------------- device side
 #ifdef __CUDACC__
@@ -197,26 +193,6 @@ __device__ __forceinline__ Where locate(const SlabGrid& g, uint32_t gw) {
   g.heads.divmod(slab_in_lj, w.kv, w.h);
   w.slab = static_cast<int64_t>(lj) * (2 * g.heads.d) + slab_in_lj;
   return w;
-}
-
-// Decompose a global sub-slab index into (layer, block, kv, head, sub).
-struct SlabCoord {
-  int64_t slab;  // ((l * n_blocks + j) * 2 + kv) * H + h
-  int32_t l, j, kv, h, sub;
-};
-
-__device__ __forceinline__ SlabCoord slab_coord(int64_t gw, int H, int n_blocks, int wps) {
-  SlabCoord c;
-  c.slab = gw / wps;
-  c.sub = static_cast<int32_t>(gw - c.slab * wps);
-  int64_t r = c.slab;
-  c.h = static_cast<int32_t>(r % H);
-  r /= H;
-  c.kv = static_cast<int32_t>(r & 1);
-  r >>= 1;
-  c.j = static_cast<int32_t>(r % n_blocks);
-  c.l = static_cast<int32_t>(r / n_blocks);
-  return c;
 }
 
 // 8 consecutive elements of a source/destination dtype, kept as raw 16-byte words.
@@ -271,31 +247,6 @@ __device__ __forceinline__ void raw8_to_float(const Raw8<T>& r, float (&x)[8]) {
       x[2 * i] = f.x;
       x[2 * i + 1] = f.y;
     }
-  }
-}
-
-// Largest |x| bit pattern over the 8 elements, as an fp32 value (exact:
-// clearing sign bits and comparing magnitudes as unsigned integers is
-// monotone for finite values).
-template <typename T>
-__device__ __forceinline__ float raw8_absmax(const Raw8<T>& r) {
-  if constexpr (sizeof(T) == 4) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      m = max(m, r.w[i].x & 0x7fffffffu);
-      m = max(m, r.w[i].y & 0x7fffffffu);
-      m = max(m, r.w[i].z & 0x7fffffffu);
-      m = max(m, r.w[i].w & 0x7fffffffu);
-    }
-    return __uint_as_float(m);
-  } else {
-    uint32_t m = __vmaxu2(__vmaxu2(r.w[0].x & 0x7fff7fffu, r.w[0].y & 0x7fff7fffu),
-                          __vmaxu2(r.w[0].z & 0x7fff7fffu, r.w[0].w & 0x7fff7fffu));
-    uint32_t hi = m >> 16, lo = m & 0xffffu;
-    uint32_t b = max(hi, lo);
-    float2 f = u32_to_float2(b, static_cast<const T*>(nullptr));
-    return f.x;
   }
 }
 
@@ -359,29 +310,6 @@ __device__ __forceinline__ void raw8_to_float2(const Raw8<T>& r, float2 (&x)[4])
   for (int i = 0; i < 4; ++i) x[i] = make_float2(f[2 * i], f[2 * i + 1]);
 }
 
-// Store 8 fp32 values to 8 destination elements, rounding to nearest even.
-__device__ __forceinline__ void store8(float* p, const float (&y)[8]) {
-  __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
-  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(y[4], y[5], y[6], y[7]));
-}
-__device__ __forceinline__ void store8(__half* p, const float (&y)[8]) {
-  uint32_t u[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __half2 h = __floats2half2_rn(y[2 * i], y[2 * i + 1]);
-    memcpy(&u[i], &h, 4);
-  }
-  __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
-}
-__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&y)[8]) {
-  uint32_t u[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
-    memcpy(&u[i], &h, 4);
-  }
-  __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
-}
 
 __device__ __forceinline__ void flag_error(int32_t* err, int bits) {
   if (bits) atomicOr(err, bits);
