@@ -272,6 +272,9 @@ def run_ours(args):
     cpu = None
     if "cpu" in args.legs and rank == 0 and world == 1:
         cpu = cpu_baseline(w, blk, budget_s=args.cpu_seconds)
+        if args.cpu_procs != 1:
+            procs, nb = parallel_oracle_shape(w, blk, cpu, args.cpu_seconds, max(args.cpu_procs, 0))
+            cpu["parallel"] = cpu_baseline_parallel(w, blk, nb, procs)
 
     if rank == 0:
         line = {
@@ -488,7 +491,91 @@ def cpu_baseline(w, blk, budget_s=15.0):
     return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"1 of {w.L} layers x {nb} of {blk.nb} blocks ({toks} tokens) of qwen3_8b, "
                       f"encode FP8 + table + fetch, float64 numpy, one thread; {t:.1f} s",
-            "tokens_per_s": toks / t}
+            "tokens_per_s": toks / t, "sample_blocks": nb, "seconds": t}
+
+
+def _oracle_worker(i, w, blk, nb, barrier, out):
+    """One process of the parallel oracle leg: its own seeded sample (a
+    different layer's draw), then one timed oracle pass once every process
+    has its sample ready."""
+    try:
+        k, v = oracle_sample(w, blk, nb, seed=1 + i)
+        barrier.wait(timeout=600)
+        t0 = time.perf_counter()
+        time_oracle_step(w, blk, k, v)
+        out.put((i, t0, time.perf_counter()))
+    except Exception as e:                                  # reported by the parent
+        out.put((i, None, repr(e)))
+
+
+def cpu_baseline_parallel(w, blk, nb, procs):
+    """The same oracle pass run by `procs` single-threaded processes at once,
+    one sample (one layer's blocks) each: aggregate bytes / wall time from the
+    first start to the last end.  Processes are spawned (never forked after
+    CUDA work); BLAS and OpenMP pools are pinned to one thread each."""
+    import multiprocessing as mp
+    import queue
+    ctx = mp.get_context("spawn")
+    barrier, out = ctx.Barrier(procs), ctx.Queue()
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    os.environ.update({k: "1" for k in saved})
+    ps = [ctx.Process(target=_oracle_worker, args=(i, w, blk, nb, barrier, out)) for i in range(procs)]
+    res, why = {}, None
+    try:
+        for pr in ps:
+            pr.start()
+        deadline = time.monotonic() + 900
+        while len(res) < procs and why is None:
+            try:
+                r = out.get(timeout=1.0)
+                res[r[0]] = r
+            except queue.Empty:
+                # a process that ended without reporting (killed, failed to start)
+                dead = [i for i, pr in enumerate(ps) if pr.exitcode is not None and i not in res]
+                if dead:
+                    why = f"process {dead[0]} exited with code {ps[dead[0]].exitcode}"
+                elif time.monotonic() > deadline:
+                    why = "timeout"
+    finally:
+        for k, val in saved.items():
+            if val is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = val
+        for pr in ps:
+            if why is not None and pr.is_alive():
+                pr.terminate()
+            pr.join(timeout=60)
+            if pr.is_alive():
+                pr.terminate()
+    failed = [r[2] for r in res.values() if r[1] is None]
+    if why is not None or failed:
+        return {"unavailable": "a worker failed: " + (why or failed[0])}
+    res = list(res.values())
+    wall = max(r[2] for r in res) - min(r[1] for r in res)
+    b, toks = sample_bytes(w, blk, nb)
+    return {"value": procs * b / wall / 1e9, "unit": "GB/s", "cores": procs, "kind": "oracle",
+            "sample": f"{procs} processes x 1 layer x {nb} of {blk.nb} blocks ({toks} tokens each) "
+                      f"of qwen3_8b, encode FP8 + table + fetch, float64 numpy, one thread each; "
+                      f"{wall:.1f} s wall",
+            "tokens_per_s": procs * toks / wall}
+
+
+def parallel_oracle_shape(w, blk, single, budget_s, procs=0):
+    """Processes and blocks per process for the parallel oracle leg: one per
+    core of this process's affinity (or `procs`), each sample sized for about
+    half the single-thread budget, and the set held to half the free host
+    memory (about 4 MB of float64 working set per 16-token block)."""
+    cores = procs or len(os.sched_getaffinity(0))
+    try:
+        free = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        free = 16 << 30
+    per_block = 4e6 * blk.B / 16
+    nb_time = int(single["sample_blocks"] * budget_s / 2 / max(single["seconds"], 1e-3))
+    nb = max(16, min(blk.nb, nb_time))
+    cores = max(1, min(cores, int(free / 2 / (per_block * nb))))
+    return cores, nb
 
 
 def run_reference(args):
@@ -737,6 +824,9 @@ def main(argv=None):
     ap.add_argument("--legs", default="device,e2e,cpu", help="comma list of: device, e2e, cpu")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-procs", type=int, default=0,
+                    help="processes of the parallel oracle leg: 0 = one per core of the affinity "
+                         "mask (bounded by host memory), 1 = skip it")
     ap.add_argument("--ref-blocks", type=int, default=16)
     ap.add_argument("--wire", choices=["int4", "fp8"], default="int4", help="ragged workload's wire format")
     ap.add_argument("--codec", choices=sorted(CODECS), default="fp8",

@@ -1,0 +1,25 @@
+"""The parallel oracle timing leg of bench.py (host only): spawned
+single-threaded processes each time one oracle pass on their own sample, and
+the leg reports aggregate bytes over the wall time."""
+import bench
+import workloads
+
+
+def test_parallel_oracle_leg_runs_and_reports():
+    w = workloads.qwen3_8b()
+    blk = w.blocks[0]
+    r = bench.cpu_baseline_parallel(w, blk, nb=4, procs=2)
+    assert "unavailable" not in r, r
+    assert r["cores"] == 2 and r["kind"] == "oracle" and r["unit"] == "GB/s"
+    assert r["value"] > 0 and r["tokens_per_s"] > 0
+    assert "2 processes x 1 layer x 4 of 2048 blocks" in r["sample"]
+
+
+def test_parallel_oracle_shape_is_bounded():
+    w = workloads.qwen3_8b()
+    blk = w.blocks[0]
+    single = {"sample_blocks": 2048, "seconds": 4.0}
+    procs, nb = bench.parallel_oracle_shape(w, blk, single, budget_s=15.0, procs=4)
+    assert 1 <= procs <= 4 and 16 <= nb <= blk.nb
+    procs, nb = bench.parallel_oracle_shape(w, blk, {"sample_blocks": 16, "seconds": 100.0}, 15.0, 3)
+    assert nb == 16
