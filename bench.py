@@ -606,6 +606,169 @@ def run_reference(args):
     }))
 
 
+# ------------------------------------------------------------------ small workloads
+SMALL_WIRES = ("fp8", "int4", "fp8_rows")
+
+
+def small_bytes(w, blk, wire):
+    """Algorithmic bytes of one pass (all layers) of a small workload."""
+    if wire != "int4":
+        return algorithmic_bytes(w, blk, wire)
+    L, H, d, T, NB = w.L, w.H, w.d, blk.tokens(), blk.nb
+    src_b = {"f32": 4, "f16": 2, "bf16": 2}[w.src_dtype]
+    out_b = {"f32": 4, "f16": 2, "bf16": 2}[w.out_dtype]
+    kv_elems = 2 * L * T * H * d
+    wire_b = kv_elems // 2 + 2 * L * T * H * (d // 32) * 2      # g32 nibbles + fp16 scales
+    n_distinct = len(np.unique(blk.delta_m))
+    table = n_distinct * (d // 2) * 8
+    return {"encode": kv_elems * src_b + wire_b + NB * 4, "table": table + n_distinct * 4,
+            "fetch": wire_b + kv_elems * out_b + table + NB * 3 * 4}
+
+
+def oracle_small(w, blk, k, v, wire):
+    """The float64 oracle over the whole small workload for one wire."""
+    from oracle import paged, rope
+    th = rope.inv_freq(w.d, w.rope_base)
+    t0 = time.perf_counter()
+    if wire == "fp8":
+        codes, scales = paged.encode_fp8(k, v, blk.src_slots, blk.n_valid)
+        vals = paged.decode_fp8(codes, scales)
+    elif wire == "int4":
+        codes, scales = paged.encode_int4(k, v, blk.src_slots, blk.n_valid, 32, "f16")
+        vals = paged.decode_int4(codes, scales, 32)
+    else:
+        codes, scales = paged.encode_fp8_rows(k, v, blk.src_slots, blk.n_valid, "f16")
+        vals = paged.decode_fp8_rows(codes, scales)
+    paged.delta_sincos_table(np.unique(blk.delta_m), th)
+    out = np.zeros((w.L, blk.num_dst_slots, blk.B, w.H, w.d))
+    paged.fetch_rotate_scatter(vals, blk.delta_m, th, w.pairing, blk.dst_slots, out, out,
+                               w.out_dtype, n_valid=blk.n_valid)
+    return time.perf_counter() - t0
+
+
+def run_small(args):
+    """The small workloads (tiny, gqa_reorder): every wire's encode + table +
+    fetch over all layers, with L2 flushed before every timed pass (their
+    working sets fit in L2), and the oracle over the same inputs in full."""
+    import torch
+    import __graft_entry__
+    import workloads
+    from kv_cache_quantization_hc_gb300 import path as kvpath
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+    w, _ = workloads.WORKLOADS[args.workload]()
+    blk = w.blocks[0]
+    stream = torch.cuda.current_stream(device)
+    src_k = workloads.device_pool(w, blk, range(w.L), 0, device)
+    src_v = workloads.device_pool(w, blk, range(w.L), 1, device)
+    shape = (w.L, blk.num_dst_slots, blk.B, w.H, w.d)
+    dst_k = torch.empty(shape, dtype=workloads.torch_dtype(w.out_dtype), device=device)
+    dst_v = torch.empty_like(dst_k)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=device)
+    peak, peak_kind = measured_peaks()
+    res = {}
+    with ClockSampler(local) as clocks:
+        for wire in SMALL_WIRES:
+            p = kvpath.from_blocks(w, blk, wire, device=device, scale_dtype="f16")
+            nbytes = small_bytes(w, blk, wire)
+
+            def step(ev=None):
+                if ev: ev[0].record(stream)
+                p.encode(src_k, src_v, stream=stream)
+                if ev: ev[1].record(stream)
+                p.build_table(stream=stream)
+                if ev: ev[2].record(stream)
+                p.fetch(dst_k, dst_v, stream=stream)
+                if ev: ev[3].record(stream)
+
+            for _ in range(args.warmup):
+                flush.zero_()
+                step()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+            torch.cuda.synchronize(device)
+            for e in evs:
+                flush.zero_()
+                step(e)
+            torch.cuda.synchronize(device)
+            if p.error_bits():
+                raise RuntimeError(f"device error flag {p.error_bits()}")
+            t = {"encode": [], "table": [], "fetch": [], "step": []}
+            for e in evs:
+                t["encode"].append(e[0].elapsed_time(e[1]) / 1e3)
+                t["table"].append(e[1].elapsed_time(e[2]) / 1e3)
+                t["fetch"].append(e[2].elapsed_time(e[3]) / 1e3)
+                t["step"].append(e[0].elapsed_time(e[3]) / 1e3)
+            kern = {k: {"median_us": statistics.median(t[k]) * 1e6, "min_us": min(t[k]) * 1e6,
+                        "bytes_per_launch": nbytes[k],
+                        "gbs": nbytes[k] / statistics.median(t[k]) / 1e9} for k in nbytes}
+            step_bytes = sum(nbytes.values())
+            med = statistics.median(t["step"])
+            # the same pass as a CUDA graph (table on a side branch, overlapping the encode)
+            g = p.capture(src_k, src_v, dst_k, dst_v)
+            for _ in range(args.warmup):
+                flush.zero_()
+                g.replay()
+            gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+            for e in gev:
+                flush.zero_()
+                e[0].record(stream)
+                g.replay()
+                e[1].record(stream)
+            torch.cuda.synchronize(device)
+            if p.error_bits():
+                raise RuntimeError(f"device error flag {p.error_bits()}")
+            gt = [e[0].elapsed_time(e[1]) / 1e3 for e in gev]
+            gmed = statistics.median(gt)
+            res[wire] = {"gbs": step_bytes / gmed / 1e9, "hbm_frac": step_bytes / gmed / 1e9 / peak,
+                         "median_step_us": gmed * 1e6, "min_step_us": min(gt) * 1e6,
+                         "bytes_per_step": step_bytes, "tokens_per_s": blk.tokens() * w.L / gmed,
+                         "eager": {"gbs": step_bytes / med / 1e9, "median_step_us": med * 1e6,
+                                   "kernels": kern}}
+            del g, p
+    cpu = None
+    if "cpu" in args.legs and rank == 0:
+        k = src_k.double().cpu().numpy()
+        v = src_v.double().cpu().numpy()
+        cpu = {}
+        for wire in SMALL_WIRES:
+            ts = oracle_small(w, blk, k, v, wire)
+            cpu[wire] = {"value": sum(small_bytes(w, blk, wire).values()) / ts / 1e9, "unit": "GB/s",
+                         "seconds": ts}
+        cpu = {"value": cpu["fp8"]["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole workload ({w.L} layers x {blk.nb} blocks), float64 numpy, "
+                         f"one thread", "wires": cpu}
+    if rank == 0:
+        fp8 = res["fp8"]
+        kern = fp8["eager"]["kernels"]
+        dom = max(("encode", "fetch"), key=lambda k: kern[k]["median_us"])
+        achieved = kern[dom]["gbs"]
+        print(json.dumps({
+            "metric": METRIC, "value": fp8["gbs"], "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": fp8["median_step_us"] / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.L} layers x {w.H} KV heads x d{w.d}, "
+                                   f"{blk.tokens()} tokens, block {blk.B}, {w.src_dtype} -> wire -> "
+                                   f"{w.out_dtype}", "value_wire": "fp8",
+                       "l2": f"flushed before every timed pass ({2 * l2 >> 20} MB write, not timed)",
+                       "timing": "median of per-pass CUDA events; value: the pass replayed as a "
+                                 "CUDA graph (KVPath.capture); wires.*.eager: the three calls "
+                                 "launched one by one, timed per kernel"},
+            "wires": res,
+            "roofline": {"kernel": {"encode": "k_encode", "fetch": "k_fetch"}[dom], "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "note": "launch-bound: the whole pass moves a few tens of MB"},
+            "gpu_launches": 2 * 3 * args.steps * len(SMALL_WIRES),
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+        }))
+
+
 # ------------------------------------------------------------------ per-layer workloads
 def layered_bytes(w, blk, wire, group=32):
     """Algorithmic bytes of one layer's encode and fetch for one block size."""
@@ -815,7 +978,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling a smaller case)")
-    ap.add_argument("--workload", choices=["qwen3_8b", "llama3_70b", "ragged", "blend", "hashing"],
+    ap.add_argument("--workload", choices=["qwen3_8b", "llama3_70b", "ragged", "blend", "hashing",
+                                           "tiny", "gqa_reorder"],
                     default="qwen3_8b",
                     help="qwen3_8b: the step the JSON line reports by default; llama3_70b / ragged "
                          "time the per-layer calls of the layer-streamed and ragged workloads; blend "
@@ -842,6 +1006,8 @@ def main(argv=None):
         run_blend(args)
     elif args.workload == "hashing":
         run_hashing(args)
+    elif args.workload in ("tiny", "gqa_reorder"):
+        run_small(args)
     elif args.workload != "qwen3_8b":
         run_layered(args)
     else:

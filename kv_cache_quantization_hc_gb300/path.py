@@ -91,6 +91,40 @@ class KVPath:
                                    self.dst_slots, self.n_valid, self.nb, dst_k, dst_v, desc,
                                    self.err, stream)
 
+    def step(self, src_k, src_v, dst_k, dst_v, stream=None, side=None):
+        """One pass: encode, then fetch, on `stream` (default: the current
+        stream). The table depends only on delta-m, so it is built on the
+        `side` stream (default: a stream of this path), overlapping the
+        encode. The side stream first waits for the work already queued on
+        `stream`, since an earlier fetch may still read the table. The fetch
+        waits for the table."""
+        stream = torch.cuda.current_stream(self.table.device) if stream is None else stream
+        if side is None:
+            if getattr(self, "_side", None) is None:
+                self._side = torch.cuda.Stream(device=self.table.device)
+            side = self._side
+        queued, built = torch.cuda.Event(), torch.cuda.Event()
+        queued.record(stream)
+        side.wait_event(queued)
+        self.build_table(stream=side)
+        built.record(side)
+        self.encode(src_k, src_v, stream=stream)
+        stream.wait_event(built)
+        self.fetch(dst_k, dst_v, stream=stream)
+
+    def capture(self, src_k, src_v, dst_k, dst_v):
+        """A CUDA graph of `step` over these buffers: replaying it runs the
+        three kernels with no host work per launch, which is what bounds calls
+        of a few tens of MB. The buffers must stay alive and in place while
+        the graph is used."""
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=self.table.device)
+        side = torch.cuda.Stream(device=self.table.device)
+        cap.wait_stream(torch.cuda.current_stream(self.table.device))
+        with torch.cuda.graph(g, stream=cap):
+            self.step(src_k, src_v, dst_k, dst_v, stream=cap, side=side)
+        return g
+
     def crc32(self, out=None, stream=None):
         """CRC-32 of every (layer, block)'s wire bytes: its codes for K and V,
         then its scales (device uint32 [n_layers * n_blocks], layer-major)."""
