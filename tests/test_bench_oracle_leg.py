@@ -23,3 +23,13 @@ def test_parallel_oracle_shape_is_bounded():
     assert 1 <= procs <= 4 and 16 <= nb <= blk.nb
     procs, nb = bench.parallel_oracle_shape(w, blk, {"sample_blocks": 16, "seconds": 100.0}, 15.0, 3)
     assert nb == 16
+
+
+def test_parallel_oracle_leg_reports_a_failing_worker():
+    """A worker that raises (here: an unknown source dtype) makes the leg an
+    `unavailable` object instead of a number, without hanging the bench."""
+    import copy
+    w = copy.copy(workloads.qwen3_8b())
+    w.src_dtype = "no-such-dtype"
+    r = bench.cpu_baseline_parallel(w, w.blocks[0], nb=4, procs=2)
+    assert "unavailable" in r and "value" not in r, r
