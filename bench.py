@@ -787,8 +787,13 @@ def layered_bytes(w, blk, wire, group=32):
 
 
 def run_layered(args):
-    """Per-layer calls: every layer is encoded (main stream) and then fetched
-    (on a side stream, after an event), as a layer-streamed fetch runs."""
+    """Per-layer calls: every layer is encoded on an encode stream and then
+    fetched on a fetch stream (after an event), as a layer-streamed fetch runs.
+    With --layer-streams K, layer l uses encode stream l % K and fetch stream
+    l % K, so neighbouring layers' calls may overlap. Each block size keeps a
+    ring of 2K wire buffers: layer l encodes into slot l % 2K only after the
+    fetch that last read that slot has finished. Each fetch stream writes its
+    own destination pool."""
     import torch
     import __graft_entry__
     import workloads
@@ -802,36 +807,50 @@ def run_layered(args):
     if args.layers:
         w.L = args.layers
     wire = "fp8" if args.workload == "llama3_70b" else args.wire
+    K = max(1, args.layer_streams)
+    R = 2 * K
     main = torch.cuda.current_stream(device)
-    side = torch.cuda.Stream(device=device)
+    enc_streams = [main] + [torch.cuda.Stream(device=device) for _ in range(K - 1)]
+    fet_streams = [torch.cuda.Stream(device=device) for _ in range(K)]
     groups = []
     for blk in w.blocks:
         p = kvpath.from_blocks(w, blk, wire, device=device, n_layers=1, scale_dtype="f16")
         src_k = workloads.device_pool(w, blk, range(0, 1), 0, device)
         src_v = workloads.device_pool(w, blk, range(0, 1), 1, device)
         shape = (1, blk.num_dst_slots, blk.B, w.H, w.d)
-        dst_k = torch.empty(shape, dtype=workloads.torch_dtype(w.out_dtype), device=device)
-        dst_v = torch.empty_like(dst_k)
+        dst = [(torch.empty(shape, dtype=workloads.torch_dtype(w.out_dtype), device=device),
+                torch.empty(shape, dtype=workloads.torch_dtype(w.out_dtype), device=device))
+               for _ in range(K)]
+        ring = [(torch.empty_like(p.codes), None if p.scales is None else torch.empty_like(p.scales))
+                for _ in range(R)]
         p.build_table(stream=main)
-        groups.append((blk, p, src_k, src_v, dst_k, dst_v, layered_bytes(w, blk, wire)))
-    evs = []
+        groups.append((blk, p, src_k, src_v, dst, ring, layered_bytes(w, blk, wire)))
 
     def step(record):
+        for st in enc_streams[1:] + fet_streams:
+            st.wait_stream(main)
+        fetched = {}
         for layer in range(w.L):
-            for gi, (blk, p, sk, sv, dk, dv, _) in enumerate(groups):
+            es, fs = enc_streams[layer % K], fet_streams[layer % K]
+            for gi, (blk, p, sk, sv, dst, ring, _) in enumerate(groups):
                 e = record[layer][gi] if record else None
-                if e: e[0].record(main)
-                p.encode(sk, sv, stream=main)
-                if e: e[1].record(main)
+                codes, scales = ring[layer % R]
+                if layer >= R:                       # the slot's previous reader is done
+                    es.wait_event(fetched[(layer - R, gi)])
+                if e: e[0].record(es)
+                p.encode(sk, sv, stream=es, codes=codes, scales=scales)
+                if e: e[1].record(es)
                 done = torch.cuda.Event()
-                done.record(main)
-                side.wait_event(done)
-                if e: e[2].record(side)
-                p.fetch(dk, dv, stream=side)
-                if e: e[3].record(side)
-        j = torch.cuda.Event()
-        j.record(side)
-        main.wait_event(j)
+                done.record(es)
+                fs.wait_event(done)
+                dk, dv = dst[layer % K]
+                if e: e[2].record(fs)
+                p.fetch(dk, dv, stream=fs, codes=codes, scales=scales)
+                if e: e[3].record(fs)
+                fetched[(layer, gi)] = torch.cuda.Event()
+                fetched[(layer, gi)].record(fs)
+        for st in enc_streams[1:] + fet_streams:
+            main.wait_stream(st)
 
     for _ in range(args.warmup):
         step(None)
@@ -868,10 +887,11 @@ def run_layered(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.L} layers, per-layer encode (main stream) + fetch "
-                               f"(side stream), wire {wire}, blocks "
+        "config": {"workload": f"{w.name}: {w.L} layers, per-layer encode + fetch on "
+                               f"{K} encode / {K} fetch stream(s), wire {wire}, blocks "
                                + "/".join(f"{g[0].nb}xB{g[0].B}" for g in groups),
-                   "tokens": tokens, "calls_per_step": 2 * w.L * len(groups)},
+                   "tokens": tokens, "calls_per_step": 2 * w.L * len(groups),
+                   "layer_streams": K, "wire_ring": R},
         "tokens_per_s": tokens * args.steps / total_s,
         "kernels": {"encode": {"avg_us_per_call": statistics.mean(enc_t) * 1e6, "gbs": enc_gbs,
                                "frac": enc_gbs / peak},
@@ -993,6 +1013,8 @@ def main(argv=None):
                          "mask (bounded by host memory), 1 = skip it")
     ap.add_argument("--ref-blocks", type=int, default=16)
     ap.add_argument("--wire", choices=["int4", "fp8"], default="int4", help="ragged workload's wire format")
+    ap.add_argument("--layer-streams", type=int, default=2,
+                    help="per-layer workloads: encode and fetch streams the layers alternate over")
     ap.add_argument("--codec", choices=sorted(CODECS), default="fp8",
                     help="wire of the qwen3_8b step: per-block-head FP8 (default) or per-row FP8")
     ap.add_argument("--crc", action="store_true",
