@@ -22,9 +22,14 @@ LIB = os.path.join(PKG, "libhc.so")
 SOURCES = ["api.cu", "encode.cu", "encode_rows.cu", "fetch_fp8.cu", "fetch_fp8_rows.cu",
            "fetch_int4.cu", "fetch_raw.cu", "table.cu", "crc32.cu", "select.cu",
            "hash.cpp"]
-HEADERS = [os.path.join(CSRC, h) for h in ("hc_internal.cuh", "fetch_impl.cuh", "encode_common.cuh",
-                                            "fastdiv.h")] + [
-    os.path.join(INCLUDE, "hc.h")]
+
+
+def _headers():
+    """Every header the translation units may include: all of csrc/'s, and hc.h."""
+    hs = sorted(f for f in os.listdir(CSRC) if f.endswith((".h", ".cuh")))
+    return [os.path.join(CSRC, h) for h in hs] + [os.path.join(INCLUDE, "hc.h")]
+
+
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 
@@ -40,7 +45,7 @@ def _nvcc():
 
 def _stamp(extra_flags):
     h = hashlib.sha256()
-    for p in [os.path.join(CSRC, s) for s in SOURCES] + HEADERS:
+    for p in [os.path.join(CSRC, s) for s in SOURCES] + _headers():
         with open(p, "rb") as f:
             h.update(p.encode() + b"\0" + f.read())
     h.update(" ".join(FLAGS + list(extra_flags)).encode())
