@@ -1,0 +1,39 @@
+"""bench.py's own arm on a small case (2 of the 36 layers): one JSON line with
+the contract's keys - roofline of the dominant kernel against the measured
+peak, the end-to-end leg through host buffers with its byte counts, the
+launch count and the clock samples."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_bench_prints_the_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--layers", "2",
+                        "--steps", "3", "--warmup", "3", "--legs", "device,e2e", "--e2e-steps", "2"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "gpu_launches", "clocks", "e2e"):
+        assert key in d, key
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
+    assert d["config"]["workload"].startswith("qwen3_8b") and d["config"]["layers"] == 2
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    assert rf["traffic"] is None          # profiles/ hold the 36-layer launch, not this one
+    assert d["gpu_launches"] == 3 * 3
+    e = d["e2e"]
+    assert e["value"] > 0 and e["unit"] == "GB/s"
+    src = 2 * 2 * 2048 * 16 * 8 * 128 * 2             # K and V, 2 layers, fp16
+    assert e["h2d_bytes_per_step"] >= src and e["d2h_bytes_per_step"] >= src
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
