@@ -140,3 +140,21 @@ def test_host_validation_of_fused_crc(lib):
     assert e(A, A, P(good), A, None, 1, A, A, None, A, None) == hc.HC_ERR_INVALID_ARG     # no crc
     assert e(A, A, P(good), A, None, 1, A, A, A + 2, A, None) == hc.HC_ERR_INVALID_ARG    # alignment
     assert e(A, A, P(good), A, None, 0, A, A, A, A, None) == hc.HC_OK
+
+
+def test_host_rejects_grids_past_32_bit_indexing(lib):
+    """2^31 or more 16-token sub-slabs in one call would overflow the kernels'
+    32-bit sub-slab index: every entry point rejects it before any CUDA call."""
+    from kv_cache_quantization_hc_gb300 import hc
+    A = 1 << 20
+    P = ctypes.byref
+    slot = 16 * 8 * 128
+    # 2^14 layers x 2^13 blocks x 2 (K, V) x 8 heads x 1 sub-slab = 2^31
+    big = hc.hc_paged_desc(1 << 14, 8, 128, 16, 1 << 13, hc.HC_BF16, slot, slot << 13)
+    nb = 1 << 13
+    assert lib.hc_encode_fp8(A, A, P(big), A, None, nb, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    assert lib.hc_encode_fp8_crc(A, A, P(big), A, None, nb, A, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    assert lib.hc_encode_int4(A, A, P(big), A, None, nb, 32, hc.HC_F16, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    assert lib.hc_encode_fp8_rows(A, A, P(big), A, None, nb, hc.HC_F16, A, A, A, None) == hc.HC_ERR_INVALID_ARG
+    f = lib.hc_fetch_rotate_scatter
+    assert f(0, A, A, 32, hc.HC_F16, A, A, 1, 0, A, None, nb, A, A, P(big), A, None) == hc.HC_ERR_INVALID_ARG
