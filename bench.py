@@ -909,7 +909,6 @@ def run_blend(args):
     import torch
     import __graft_entry__
     import workloads
-    from oracle import blend
     from kv_cache_quantization_hc_gb300 import hc
 
     rank, world, local = dist_env()
@@ -918,7 +917,7 @@ def run_blend(args):
     __graft_entry__.build()
     w = workloads.blend_selection()
     cached, fresh = workloads.blend_hidden(w, device)
-    k = blend.default_k(w.n_tokens)
+    k = hc.selection_size(w.n_tokens)
     drift = torch.empty((w.n_seq, w.n_tokens), dtype=torch.float32, device=device)
     sel = torch.empty((w.n_seq, k), dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)

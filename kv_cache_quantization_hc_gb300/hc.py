@@ -168,10 +168,19 @@ def hc_drift_select(h_cached, h_fresh, dtype, n_seq, n_tokens, hidden, token_str
         _ptr(drift), _ptr(selected), _stream(stream)))
 
 
-def drift_select(h_cached, h_fresh, k, drift=None, selected=None, stream=None):
+def selection_size(n_tokens, fraction=0.15):
+    """Tokens a sequence recomputes: ceil(fraction * n_tokens), at least 1,
+    with the fraction taken exactly as the decimal it is written as (0.15 of
+    100 tokens is 15, not 16)."""
+    from fractions import Fraction
+    f = Fraction(str(fraction))
+    return max(1, -((-f.numerator * int(n_tokens)) // f.denominator))
+
+
+def drift_select(h_cached, h_fresh, k=None, drift=None, selected=None, stream=None):
     """hc_drift_select on tensors shaped [n_seq, n_tokens, hidden] (or
     [n_tokens, hidden]); returns (drift [n_seq, n_tokens] f32, selected
-    [n_seq, k] int32)."""
+    [n_seq, k] int32).  k defaults to selection_size(n_tokens)."""
     import torch
     if h_cached.dim() == 2:
         h_cached, h_fresh = h_cached.unsqueeze(0), h_fresh.unsqueeze(0)
@@ -180,6 +189,7 @@ def drift_select(h_cached, h_fresh, k, drift=None, selected=None, stream=None):
     if h_cached.stride(2) != 1:
         raise ValueError("the hidden dimension must be contiguous")
     n_seq, n_tokens, hidden = h_cached.shape
+    k = selection_size(n_tokens) if k is None else k
     dev = h_cached.device
     drift = torch.empty((n_seq, n_tokens), dtype=torch.float32, device=dev) if drift is None else drift
     selected = torch.empty((n_seq, k), dtype=torch.int32, device=dev) if selected is None else selected
