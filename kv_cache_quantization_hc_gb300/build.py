@@ -5,6 +5,7 @@ static CUDA runtime, so the library depends on no libcudart at load time.
 A stamp of the sources' hash and the flags skips rebuilding an up-to-date
 library built for this machine's architecture.
 """
+import fcntl
 import hashlib
 import os
 import platform
@@ -68,8 +69,21 @@ def _lib_matches_host(path):
 
 def build(force=False, verbose=False, extra_flags=(), out_dir=None):
     """Compile and link libhc.so; returns its path.  ``out_dir`` places the
-    objects and the library elsewhere (a variant built with extra flags)."""
+    objects and the library elsewhere (a variant built with extra flags).
+    Concurrent callers (the ranks of a torchrun job) take turns on a lock
+    file in the build directory: the first builds, the others then find the
+    stamp up to date."""
     build_dir = BUILD if out_dir is None else out_dir
+    os.makedirs(build_dir, exist_ok=True)
+    with open(os.path.join(build_dir, "lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(build_dir, force, verbose, extra_flags, out_dir)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(build_dir, force, verbose, extra_flags, out_dir):
     lib = LIB if out_dir is None else os.path.join(out_dir, "libhc.so")
     stamp = _stamp(extra_flags)
     stamp_path = os.path.join(build_dir, "stamp")
@@ -77,7 +91,6 @@ def build(force=False, verbose=False, extra_flags=(), out_dir=None):
         with open(stamp_path) as f:
             if f.read().strip() == stamp:
                 return lib
-    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
