@@ -86,6 +86,15 @@ def _ptr(x):
     return x.data_ptr()
 
 
+def _dptr(x, name):
+    """Address of a device buffer: like _ptr, but a torch tensor must live on
+    a CUDA device (the kernels dereference these pointers; a host tensor
+    would make them fault)."""
+    if x is not None and not isinstance(x, int) and not getattr(x, "is_cuda", False):
+        raise ValueError(f"{name} must be a CUDA tensor (or a device address)")
+    return _ptr(x)
+
+
 def _stream(s):
     """cudaStream_t of a torch stream; None means torch's current stream."""
     if isinstance(s, int):
@@ -130,42 +139,42 @@ def paged_desc(pool, dtype=None, n_layers=None, layer_stride=None, slot_stride=N
 def hc_encode_fp8(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes, scales, err_flag,
                   stream=None):
     _check("hc_encode_fp8", lib().hc_encode_fp8(
-        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
-        n_blocks, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
+        n_blocks, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 def hc_encode_fp8_crc(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes, scales, crc,
                       err_flag, stream=None):
     _check("hc_encode_fp8_crc", lib().hc_encode_fp8_crc(
-        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
-        n_blocks, _ptr(codes), _ptr(scales), _ptr(crc), _ptr(err_flag), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
+        n_blocks, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(crc, "crc"), _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 def hc_encode_int4(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, group, scale_dtype,
                    codes, scales, err_flag, stream=None):
     _check("hc_encode_int4", lib().hc_encode_int4(
-        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
-        n_blocks, group, scale_dtype, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
+        n_blocks, group, scale_dtype, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 def hc_encode_fp8_rows(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, scale_dtype, codes,
                        scales, err_flag, stream=None):
     _check("hc_encode_fp8_rows", lib().hc_encode_fp8_rows(
-        _ptr(paged_k), _ptr(paged_v), ctypes.byref(desc), _ptr(src_slots), _ptr(n_valid),
-        n_blocks, scale_dtype, _ptr(codes), _ptr(scales), _ptr(err_flag), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
+        n_blocks, scale_dtype, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 def hc_crc32(a, a_bytes, a_stride, b, b_bytes, b_stride, n_units, crc, stream=None):
     _check("hc_crc32", lib().hc_crc32(
-        _ptr(a), a_bytes, a_stride, _ptr(b), b_bytes, b_stride, n_units, _ptr(crc),
+        _dptr(a, "a"), a_bytes, a_stride, _dptr(b, "b"), b_bytes, b_stride, n_units, _dptr(crc, "crc"),
         _stream(stream)))
 
 
 def hc_drift_select(h_cached, h_fresh, dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
                     drift, selected, stream=None):
     _check("hc_drift_select", lib().hc_drift_select(
-        _ptr(h_cached), _ptr(h_fresh), dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
-        _ptr(drift), _ptr(selected), _stream(stream)))
+        _dptr(h_cached, "h_cached"), _dptr(h_fresh, "h_fresh"), dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
+        _dptr(drift, "drift"), _dptr(selected, "selected"), _stream(stream)))
 
 
 def selection_size(n_tokens, fraction=0.15):
@@ -224,7 +233,7 @@ def block_digests(tokens, block_size, key):
 
 def hc_build_delta_sincos(delta_m, n_distinct, d_head, rope_base, inv_freq, table, stream=None):
     _check("hc_build_delta_sincos", lib().hc_build_delta_sincos(
-        _ptr(delta_m), n_distinct, d_head, float(rope_base), _ptr(inv_freq), _ptr(table),
+        _dptr(delta_m, "delta_m"), n_distinct, d_head, float(rope_base), _dptr(inv_freq, "inv_freq"), _dptr(table, "table"),
         _stream(stream)))
 
 
@@ -232,9 +241,9 @@ def hc_fetch_rotate_scatter(wire, codes, scales, group, scale_dtype, table, delt
                             pairing, dst_slots, n_valid, n_blocks, paged_k, paged_v, desc,
                             err_flag, stream=None):
     _check("hc_fetch_rotate_scatter", lib().hc_fetch_rotate_scatter(
-        wire, _ptr(codes), _ptr(scales), group, scale_dtype, _ptr(table), _ptr(delta_idx),
-        n_distinct, pairing, _ptr(dst_slots), _ptr(n_valid), n_blocks, _ptr(paged_k),
-        _ptr(paged_v), ctypes.byref(desc), _ptr(err_flag), _stream(stream)))
+        wire, _dptr(codes, "codes"), _dptr(scales, "scales"), group, scale_dtype, _dptr(table, "table"), _dptr(delta_idx, "delta_idx"),
+        n_distinct, pairing, _dptr(dst_slots, "dst_slots"), _dptr(n_valid, "n_valid"), n_blocks, _dptr(paged_k, "paged_k"),
+        _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 # ------------------------------------------------------------- buffer shapes

@@ -158,3 +158,23 @@ def test_host_rejects_grids_past_32_bit_indexing(lib):
     assert lib.hc_encode_fp8_rows(A, A, P(big), A, None, nb, hc.HC_F16, A, A, A, None) == hc.HC_ERR_INVALID_ARG
     f = lib.hc_fetch_rotate_scatter
     assert f(0, A, A, 32, hc.HC_F16, A, A, 1, 0, A, None, nb, A, A, P(big), A, None) == hc.HC_ERR_INVALID_ARG
+
+
+def test_binding_rejects_host_tensors_for_device_buffers(lib):
+    """The kernels dereference every buffer pointer: the binding refuses a
+    host tensor before the call instead of letting a kernel fault on it."""
+    import torch
+    from kv_cache_quantization_hc_gb300 import hc
+    good = hc.hc_paged_desc(1, 8, 128, 16, 4, hc.HC_BF16, 16 * 8 * 128, 0)
+    host = torch.zeros(16, dtype=torch.int32)
+    with pytest.raises(ValueError, match="src_slots"):
+        hc.hc_encode_fp8(1 << 20, 1 << 20, good, host, None, 1, 1 << 20, 1 << 20, 1 << 20)
+    with pytest.raises(ValueError, match="codes"):
+        hc.hc_fetch_rotate_scatter(0, host, 1 << 20, 32, hc.HC_F16, 1 << 20, 1 << 20, 1, 0,
+                                   1 << 20, None, 1, 1 << 20, 1 << 20, good, 1 << 20)
+    with pytest.raises(ValueError, match="crc"):
+        hc.hc_crc32(1 << 20, 64, 64, None, 0, 0, 1, host)
+    with pytest.raises(ValueError, match="h_cached"):
+        hc.hc_drift_select(host, 1 << 20, hc.HC_BF16, 1, 16, 8, 8, 128, 2, 1 << 20, 1 << 20)
+    with pytest.raises(ValueError, match="table"):
+        hc.hc_build_delta_sincos(1 << 20, 1, 128, 1e4, None, host)
