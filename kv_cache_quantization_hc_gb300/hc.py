@@ -95,6 +95,75 @@ def _dptr(x, name):
     return _ptr(x)
 
 
+def _avail(x):
+    """Bytes reachable from a tensor's data pointer (None for a raw address
+    or NULL, which are not checked)."""
+    if x is None or isinstance(x, int):
+        return None
+    return x.untyped_storage().nbytes() - x.storage_offset() * x.element_size()
+
+
+def _need(x, nbytes, name):
+    """Refuse a tensor smaller than the bytes the call will address."""
+    a = _avail(x)
+    if a is not None and a < nbytes:
+        raise ValueError(f"{name} holds {a} bytes; the call addresses {nbytes}")
+
+
+_ES = {HC_F32: 4, HC_F16: 2, HC_BF16: 2}
+
+
+def _pool_bytes(desc):
+    """Bytes a call addresses in a paged pool described by `desc`."""
+    last = ((desc.n_layers - 1) * desc.layer_stride + (desc.num_slots - 1) * desc.slot_stride
+            + desc.block_size * desc.n_kv_heads * desc.d_head)
+    return last * _ES.get(desc.dtype, 1)
+
+
+def _wire_bytes(desc, n_blocks, wire, group, scale_dtype):
+    """(codes bytes, scales bytes) of the wire of a call on pools like `desc`."""
+    cs, cdt, ss = wire_shapes(desc.n_layers, n_blocks, desc.n_kv_heads, desc.block_size,
+                              desc.d_head, wire, group)
+    n = 1
+    for v in cs:
+        n *= v
+    codes = n * (_ES.get(desc.dtype, 1) if cdt == "paged" else 1)
+    if ss is None:
+        return codes, 0
+    m = 1
+    for v in ss:
+        m *= v
+    return codes, m * (4 if wire == HC_WIRE_FP8 or scale_dtype == HC_F32 else 2)
+
+
+def _sizes_apply(desc, n_blocks, wire, group=32):
+    """True for a call the C layer would accept on its descriptor, wire and
+    group: only then are buffer sizes checked here, so that a malformed
+    call still gets the C layer's own status."""
+    return (n_blocks > 0 and desc.dtype in _ES and desc.d_head in (64, 128)
+            and desc.block_size in (16, 32, 64, 128) and desc.n_layers >= 1
+            and desc.num_slots >= 1 and desc.n_kv_heads >= 1 and desc.slot_stride >= 0
+            and desc.layer_stride >= 0
+            and wire in (HC_WIRE_FP8, HC_WIRE_INT4, HC_WIRE_RAW, HC_WIRE_FP8_ROWS)
+            and (wire != HC_WIRE_INT4 or (group in (32, 64, 128) and group <= desc.d_head)))
+
+
+def _check_encode(desc, paged_k, paged_v, src_slots, n_valid, n_blocks, codes, scales, err_flag,
+                  wire, group=32, scale_dtype=HC_F16, crc=None):
+    if not _sizes_apply(desc, n_blocks, wire, group):
+        return
+    pool = _pool_bytes(desc)
+    _need(paged_k, pool, "paged_k")
+    _need(paged_v, pool, "paged_v")
+    _need(src_slots, 4 * n_blocks, "src_slots")
+    _need(n_valid, 4 * n_blocks, "n_valid")
+    cb, sb = _wire_bytes(desc, n_blocks, wire, group, scale_dtype)
+    _need(codes, cb, "codes")
+    _need(scales, sb, "scales")
+    _need(err_flag, 4, "err_flag")
+    _need(crc, 4 * desc.n_layers * n_blocks * 2 * desc.n_kv_heads, "crc")
+
+
 def _stream(s):
     """cudaStream_t of a torch stream; None means torch's current stream."""
     if isinstance(s, int):
@@ -138,43 +207,71 @@ def paged_desc(pool, dtype=None, n_layers=None, layer_stride=None, slot_stride=N
 # ------------------------------------------------------------- the C-ABI calls
 def hc_encode_fp8(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes, scales, err_flag,
                   stream=None):
+    _check_encode(desc, paged_k, paged_v, src_slots, n_valid, n_blocks, codes, scales, err_flag,
+                  HC_WIRE_FP8)
     _check("hc_encode_fp8", lib().hc_encode_fp8(
-        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
-        n_blocks, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc),
+        _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"), n_blocks, _dptr(codes, "codes"),
+        _dptr(scales, "scales"), _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 def hc_encode_fp8_crc(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, codes, scales, crc,
                       err_flag, stream=None):
+    _check_encode(desc, paged_k, paged_v, src_slots, n_valid, n_blocks, codes, scales, err_flag,
+                  HC_WIRE_FP8, crc=crc)
     _check("hc_encode_fp8_crc", lib().hc_encode_fp8_crc(
-        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
-        n_blocks, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(crc, "crc"), _dptr(err_flag, "err_flag"), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc),
+        _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"), n_blocks, _dptr(codes, "codes"),
+        _dptr(scales, "scales"), _dptr(crc, "crc"), _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 def hc_encode_int4(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, group, scale_dtype,
                    codes, scales, err_flag, stream=None):
+    _check_encode(desc, paged_k, paged_v, src_slots, n_valid, n_blocks, codes, scales, err_flag,
+                  HC_WIRE_INT4, group, scale_dtype)
     _check("hc_encode_int4", lib().hc_encode_int4(
-        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
-        n_blocks, group, scale_dtype, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc),
+        _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"), n_blocks, group, scale_dtype,
+        _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"),
+        _stream(stream)))
 
 
 def hc_encode_fp8_rows(paged_k, paged_v, desc, src_slots, n_valid, n_blocks, scale_dtype, codes,
                        scales, err_flag, stream=None):
+    _check_encode(desc, paged_k, paged_v, src_slots, n_valid, n_blocks, codes, scales, err_flag,
+                  HC_WIRE_FP8_ROWS, 32, scale_dtype)
     _check("hc_encode_fp8_rows", lib().hc_encode_fp8_rows(
-        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"),
-        n_blocks, scale_dtype, _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"), _stream(stream)))
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc),
+        _dptr(src_slots, "src_slots"), _dptr(n_valid, "n_valid"), n_blocks, scale_dtype,
+        _dptr(codes, "codes"), _dptr(scales, "scales"), _dptr(err_flag, "err_flag"),
+        _stream(stream)))
 
 
 def hc_crc32(a, a_bytes, a_stride, b, b_bytes, b_stride, n_units, crc, stream=None):
+    if n_units > 0 and a_bytes >= 0 and a_stride >= a_bytes and b_bytes >= 0 and b_stride >= b_bytes:
+        _need(a, (n_units - 1) * a_stride + a_bytes, "a")
+        if b_bytes:
+            _need(b, (n_units - 1) * b_stride + b_bytes, "b")
+        _need(crc, 4 * n_units, "crc")
     _check("hc_crc32", lib().hc_crc32(
-        _dptr(a, "a"), a_bytes, a_stride, _dptr(b, "b"), b_bytes, b_stride, n_units, _dptr(crc, "crc"),
-        _stream(stream)))
+        _dptr(a, "a"), a_bytes, a_stride, _dptr(b, "b"), b_bytes, b_stride, n_units,
+        _dptr(crc, "crc"), _stream(stream)))
 
 
 def hc_drift_select(h_cached, h_fresh, dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
                     drift, selected, stream=None):
+    if (n_seq > 0 and n_tokens > 0 and hidden > 0 and dtype in _ES and 0 < k <= n_tokens
+            and token_stride >= hidden and seq_stride >= n_tokens * token_stride):
+        es = _ES[dtype]
+        span = ((n_seq - 1) * seq_stride + (n_tokens - 1) * token_stride + hidden) * es
+        _need(h_cached, span, "h_cached")
+        _need(h_fresh, span, "h_fresh")
+        _need(drift, 4 * n_seq * n_tokens, "drift")
+        _need(selected, 4 * n_seq * k, "selected")
     _check("hc_drift_select", lib().hc_drift_select(
-        _dptr(h_cached, "h_cached"), _dptr(h_fresh, "h_fresh"), dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
-        _dptr(drift, "drift"), _dptr(selected, "selected"), _stream(stream)))
+        _dptr(h_cached, "h_cached"), _dptr(h_fresh, "h_fresh"), dtype, n_seq, n_tokens, hidden,
+        token_stride, seq_stride, k, _dptr(drift, "drift"), _dptr(selected, "selected"),
+        _stream(stream)))
 
 
 def selection_size(n_tokens, fraction=0.15):
@@ -232,18 +329,35 @@ def block_digests(tokens, block_size, key):
 
 
 def hc_build_delta_sincos(delta_m, n_distinct, d_head, rope_base, inv_freq, table, stream=None):
+    if n_distinct > 0 and d_head > 0 and d_head % 2 == 0:
+        _need(delta_m, 4 * n_distinct, "delta_m")
+        _need(inv_freq, 8 * (d_head // 2), "inv_freq")
+        _need(table, 8 * n_distinct * (d_head // 2), "table")
     _check("hc_build_delta_sincos", lib().hc_build_delta_sincos(
-        _dptr(delta_m, "delta_m"), n_distinct, d_head, float(rope_base), _dptr(inv_freq, "inv_freq"), _dptr(table, "table"),
-        _stream(stream)))
+        _dptr(delta_m, "delta_m"), n_distinct, d_head, float(rope_base),
+        _dptr(inv_freq, "inv_freq"), _dptr(table, "table"), _stream(stream)))
 
 
 def hc_fetch_rotate_scatter(wire, codes, scales, group, scale_dtype, table, delta_idx, n_distinct,
                             pairing, dst_slots, n_valid, n_blocks, paged_k, paged_v, desc,
                             err_flag, stream=None):
+    if _sizes_apply(desc, n_blocks, wire, group) and n_distinct > 0:
+        pool = _pool_bytes(desc)
+        _need(paged_k, pool, "paged_k")
+        _need(paged_v, pool, "paged_v")
+        cb, sb = _wire_bytes(desc, n_blocks, wire, group, scale_dtype)
+        _need(codes, cb, "codes")
+        _need(scales, sb, "scales")
+        _need(table, 8 * n_distinct * (desc.d_head // 2), "table")
+        for t, nm in ((delta_idx, "delta_idx"), (dst_slots, "dst_slots"), (n_valid, "n_valid")):
+            _need(t, 4 * n_blocks, nm)
+        _need(err_flag, 4, "err_flag")
     _check("hc_fetch_rotate_scatter", lib().hc_fetch_rotate_scatter(
-        wire, _dptr(codes, "codes"), _dptr(scales, "scales"), group, scale_dtype, _dptr(table, "table"), _dptr(delta_idx, "delta_idx"),
-        n_distinct, pairing, _dptr(dst_slots, "dst_slots"), _dptr(n_valid, "n_valid"), n_blocks, _dptr(paged_k, "paged_k"),
-        _dptr(paged_v, "paged_v"), ctypes.byref(desc), _dptr(err_flag, "err_flag"), _stream(stream)))
+        wire, _dptr(codes, "codes"), _dptr(scales, "scales"), group, scale_dtype,
+        _dptr(table, "table"), _dptr(delta_idx, "delta_idx"), n_distinct, pairing,
+        _dptr(dst_slots, "dst_slots"), _dptr(n_valid, "n_valid"), n_blocks,
+        _dptr(paged_k, "paged_k"), _dptr(paged_v, "paged_v"), ctypes.byref(desc),
+        _dptr(err_flag, "err_flag"), _stream(stream)))
 
 
 # ------------------------------------------------------------- buffer shapes

@@ -178,3 +178,48 @@ def test_binding_rejects_host_tensors_for_device_buffers(lib):
         hc.hc_drift_select(host, 1 << 20, hc.HC_BF16, 1, 16, 8, 8, 128, 2, 1 << 20, 1 << 20)
     with pytest.raises(ValueError, match="table"):
         hc.hc_build_delta_sincos(1 << 20, 1, 128, 1e4, None, host)
+
+
+def test_binding_refuses_buffers_smaller_than_the_call(lib):
+    """A buffer smaller than the bytes the call will address is refused
+    before the call (checked ahead of the device check, so it runs here).
+    A view is measured by the storage behind its data pointer."""
+    import torch
+    from kv_cache_quantization_hc_gb300 import hc
+    L, H, d, B, S, nb = 2, 8, 128, 16, 4, 3
+    slot = B * H * d
+    desc = hc.hc_paged_desc(L, H, d, B, S, hc.HC_BF16, slot, S * slot)
+    pool = torch.zeros(L * S * slot, dtype=torch.bfloat16)
+    small = torch.zeros(L * S * slot - 1, dtype=torch.bfloat16)
+    tab = torch.zeros(nb, dtype=torch.int32)
+    codes = torch.zeros(L * nb * 2 * H * B * d, dtype=torch.uint8)
+    scales = torch.zeros(L * nb * 2 * H, dtype=torch.float32)
+    err = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="paged_v holds"):
+        hc.hc_encode_fp8(pool, small, desc, tab, None, nb, codes, scales, err)
+    with pytest.raises(ValueError, match="src_slots holds"):
+        hc.hc_encode_fp8(pool, pool, desc, torch.zeros(nb - 1, dtype=torch.int32), None, nb,
+                         codes, scales, err)
+    with pytest.raises(ValueError, match="codes holds"):
+        hc.hc_encode_fp8(pool, pool, desc, tab, None, nb,
+                         torch.zeros(codes.numel() - 1, dtype=torch.uint8), scales, err)
+    with pytest.raises(ValueError, match="scales holds"):
+        hc.hc_encode_int4(pool, pool, desc, tab, None, nb, 32, hc.HC_F16,
+                          torch.zeros(codes.numel() // 2, dtype=torch.uint8),
+                          torch.zeros(3, dtype=torch.float16), err)
+    with pytest.raises(ValueError, match="crc holds"):
+        hc.hc_encode_fp8_crc(pool, pool, desc, tab, None, nb, codes, scales,
+                             torch.zeros(L * nb * 2 * H - 1, dtype=torch.int32), err)
+    with pytest.raises(ValueError, match="table holds"):
+        hc.hc_fetch_rotate_scatter(hc.HC_WIRE_FP8, codes, scales, 32, hc.HC_F16,
+                                   torch.zeros(64 * 2 - 1, dtype=torch.float32), tab, 1, 0, tab,
+                                   None, nb, pool, pool, desc, err)
+    with pytest.raises(ValueError, match="a holds"):
+        hc.hc_crc32(torch.zeros(100, dtype=torch.uint8), 64, 64, None, 0, 0, 2, err)
+    with pytest.raises(ValueError, match="selected holds"):
+        h = torch.zeros(2 * 16 * 8, dtype=torch.bfloat16)
+        hc.hc_drift_select(h, h, hc.HC_BF16, 2, 16, 8, 8, 128, 3,
+                           torch.zeros(32, dtype=torch.float32), torch.zeros(5, dtype=torch.int32))
+    # a call whose buffers are large enough gets past the size checks, to the device check
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        hc.hc_encode_fp8(pool, pool, desc, tab, None, nb, codes, scales, err)
