@@ -381,8 +381,9 @@ def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device, dev
     public LayerStream schedule): per layer, the fp16 source is copied from
     pinned host memory, encoded and fetched, and the bf16 result copied back;
     uploads, kernels and downloads of neighbouring layers overlap on three
-    streams.  The block tables are uploaded every step as well.  Every copy is
-    inside the timed region.  `overlap` compares the step with its parts run
+    streams.  The block tables are uploaded every step as well, and the steps
+    are streamed back to back (one step's last downloads overlap the next
+    step's first uploads).  Every copy is inside the timed region.  `overlap` compares the step with its parts run
     alone (whole upload, the device step, whole download): hidden_frac is the
     share of the shorter parts' time that the pipeline hid (1 = the step takes
     only as long as its longest part)."""
@@ -408,21 +409,20 @@ def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device, dev
     h_err = torch.zeros(1, dtype=torch.int32, pin_memory=True)
     steps = max(1, min(args.steps, args.e2e_steps))
 
-    def step():
-        for d_t, h_t in zip(tables, h_tables):
-            d_t.copy_(h_t, non_blocking=True)
-        # the shuffled destination table covers every slot (checked by the
-        # full-size parity test), so the destination need not be uploaded
-        ls.run(h_src_k, h_src_v, h_dst_k, h_dst_v, h_err, preserve_dst=False)
+    def passes(n):
+        # n steps streamed back to back: every step uploads its block tables
+        # and sources and downloads its results; the shuffled destination
+        # table covers every slot (checked by the full-size parity test), so
+        # the destination need not be uploaded
+        ls.run(h_src_k, h_src_v, h_dst_k, h_dst_v, h_err, preserve_dst=False, passes=n,
+               tables=list(zip(tables, h_tables)))
 
-    for _ in range(2):
-        step()
+    passes(2)
     torch.cuda.synchronize(device)
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        step()
+    passes(steps)
     b.record(stream)
     torch.cuda.synchronize(device)
     if int(h_err.item()):
@@ -455,7 +455,8 @@ def run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device, dev
                    "hidden_frac": (serial - e2e_s) / (serial - longest) if serial > longest else None}
     return {"value": total / secs / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3,
-            "schedule": "layer-streamed: upload l+1 / compute l / download l-1 on three streams",
+            "schedule": "layer-streamed: upload l+1 / compute l / download l-1 on three streams; "
+                        "steps streamed back to back",
             "overlap": overlap}
 
 

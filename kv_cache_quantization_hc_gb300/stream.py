@@ -51,7 +51,8 @@ class LayerStream:
         self.compute = torch.cuda.Stream(device=dev)
         self.dev = dev
 
-    def run(self, h_src_k, h_src_v, h_dst_k, h_dst_v, h_err=None, preserve_dst=True):
+    def run(self, h_src_k, h_src_v, h_dst_k, h_dst_v, h_err=None, preserve_dst=True, passes=1,
+            tables=()):
         """One pass over all layers: h_src_* [L, num_slots, B, H, d] pinned host
         tensors in, h_dst_* [L, ...] pinned host tensors out.  Enqueues
         everything and returns; the caller synchronizes.  If ``h_err`` (a pinned
@@ -62,53 +63,67 @@ class LayerStream:
         default) each destination layer is first uploaded too, so slots the
         fetch does not write keep their host contents; a caller whose block
         table writes every slot of the destination can turn it off and save
-        that upload."""
+        that upload.
+
+        ``passes`` > 1 streams that many passes back to back with no join
+        between them, so one pass's last downloads overlap the next pass's
+        first uploads.  ``tables`` is a list of (device tensor, pinned host
+        tensor) pairs, such as the block tables, uploaded at the start of
+        every pass once the previous pass's last compute (which reads them)
+        has finished."""
         L = h_src_k.shape[0]
         p = self.p
-        uploaded = [None] * L
-        computed = [None] * L
-        downloaded = [None] * L
+        n = passes * L
+        uploaded = [None] * n
+        computed = [None] * n
+        downloaded = [None] * n
         cur = torch.cuda.current_stream(self.dev)
         for s in (self.up, self.down, self.compute):
             s.wait_stream(cur)
-        with torch.cuda.stream(self.compute):
-            p.build_table(stream=self.compute)
-        for layer in range(L):
-            slot = layer % self.ring
+        for it in range(n):
+            layer, slot = it % L, it % self.ring
             sk, sv = self.src[slot]
             dk, dv = self.dst[slot]
             with torch.cuda.stream(self.up):
-                if layer >= self.ring:                      # slot's previous reader done
-                    self.up.wait_event(computed[layer - self.ring])
+                if layer == 0 and tables:
+                    if it > 0:                              # the last pass's compute read them
+                        self.up.wait_event(computed[it - 1])
+                    for d_t, h_t in tables:
+                        d_t.copy_(h_t, non_blocking=True)
+                if it >= self.ring:                         # slot's previous reader done
+                    self.up.wait_event(computed[it - self.ring])
                 sk.copy_(h_src_k[layer], non_blocking=True)
                 sv.copy_(h_src_v[layer], non_blocking=True)
                 if preserve_dst:
-                    if layer >= self.ring:                  # output slot downloaded
-                        self.up.wait_event(downloaded[layer - self.ring])
+                    if it >= self.ring:                     # output slot downloaded
+                        self.up.wait_event(downloaded[it - self.ring])
                     dk.copy_(h_dst_k[layer], non_blocking=True)
                     dv.copy_(h_dst_v[layer], non_blocking=True)
-                uploaded[layer] = torch.cuda.Event()
-                uploaded[layer].record(self.up)
-            self.compute.wait_event(uploaded[layer])
-            if layer >= self.ring:                          # output slot downloaded
-                self.compute.wait_event(downloaded[layer - self.ring])
+                uploaded[it] = torch.cuda.Event()
+                uploaded[it].record(self.up)
+            self.compute.wait_event(uploaded[it])
+            if it >= self.ring:                             # output slot downloaded
+                self.compute.wait_event(downloaded[it - self.ring])
+            if layer == 0:
+                with torch.cuda.stream(self.compute):
+                    p.build_table(stream=self.compute)
             desc_s = hc.paged_desc(sk)
             desc_d = hc.paged_desc(dk)
             p.encode(sk, sv, desc=desc_s, stream=self.compute, codes=self.codes[slot],
                      scales=self.scales[slot])
             p.fetch(dk, dv, desc=desc_d, stream=self.compute, codes=self.codes[slot],
                     scales=self.scales[slot])
-            computed[layer] = torch.cuda.Event()
-            computed[layer].record(self.compute)
+            computed[it] = torch.cuda.Event()
+            computed[it].record(self.compute)
             with torch.cuda.stream(self.down):
-                self.down.wait_event(computed[layer])
+                self.down.wait_event(computed[it])
                 h_dst_k[layer].copy_(dk, non_blocking=True)
                 h_dst_v[layer].copy_(dv, non_blocking=True)
-                downloaded[layer] = torch.cuda.Event()
-                downloaded[layer].record(self.down)
+                downloaded[it] = torch.cuda.Event()
+                downloaded[it].record(self.down)
         if h_err is not None:
             with torch.cuda.stream(self.down):
-                self.down.wait_event(computed[L - 1])
+                self.down.wait_event(computed[n - 1])
                 h_err.copy_(p.err, non_blocking=True)
         for s in (self.up, self.down, self.compute):
             cur.wait_stream(s)
