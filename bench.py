@@ -274,6 +274,8 @@ def run_ours(args):
                    "min_ms": min(per[k]) * 1e3,
                    "bytes_per_launch": nbytes[k], "gbs": nbytes[k] / avg / 1e9 if avg > 0 else None}
     kern["table"]["timing"] = "time the table ends after the encode (it runs on a side stream)"
+    for k in ("encode", "fetch"):   # context tokens (all layers of the call) per second
+        kern[k]["tokens_per_s"] = blk.tokens() / (kern[k]["avg_ms"] / 1e3)
     dominant = max(("encode", "fetch"), key=lambda k: kern[k]["avg_ms"])
     kname = {"encode": "k_encode", "fetch": "k_fetch"}[dominant]
     if args.codec == "fp8_rows":
