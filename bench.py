@@ -900,8 +900,6 @@ def run_layered(args):
     step_bytes = enc_b + fet_b
     tokens = sum(g[0].tokens() for g in groups)
     peak, peak_kind = measured_peaks()
-    enc_gbs = enc_b * args.steps / sum(enc_t) / 1e9
-    fet_gbs = fet_b * args.steps / sum(fet_t) / 1e9
     print(json.dumps({
         "metric": METRIC, "value": step_bytes * args.steps / total_s / 1e9, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -913,15 +911,12 @@ def run_layered(args):
                    "tokens": tokens, "calls_per_step": 2 * w.L * len(groups),
                    "layer_streams": K, "wire_ring": R},
         "tokens_per_s": tokens * args.steps / total_s,
-        "kernels": ({"encode": {"avg_us_per_call": statistics.mean(enc_t) * 1e6, "gbs": enc_gbs,
-                                "frac": enc_gbs / peak},
-                     "fetch": {"avg_us_per_call": statistics.mean(fet_t) * 1e6, "gbs": fet_gbs,
-                               "frac": fet_gbs / peak}} if K == 1 else
-                    {"encode": {"avg_us_per_call": statistics.mean(enc_t) * 1e6},
-                     "fetch": {"avg_us_per_call": statistics.mean(fet_t) * 1e6},
-                     "note": f"calls of neighbouring layers overlap on {K} stream pairs, so a "
-                             "call's span includes time shared with others; per-call rates "
-                             "are reported with --layer-streams 1"}),
+        "kernels": {"encode": {"avg_us_per_call": statistics.mean(enc_t) * 1e6},
+                    "fetch": {"avg_us_per_call": statistics.mean(fet_t) * 1e6},
+                    "note": "a layer's fetch overlaps the next layer's encode (and, with more "
+                            "stream pairs, neighbouring layers' calls overlap each other), so a "
+                            "call's span includes time shared with other calls; the pass's rate "
+                            "is `value`, its time per layer `per_layer_us`"},
         "per_layer_us": total_s / args.steps / w.L * 1e6,
         "peak": peak, "peak_source": peak_kind, "gpu_launches": 2 * n_calls,
         "clocks": clocks.summary()}))
