@@ -666,6 +666,53 @@ def oracle_small(w, blk, k, v, wire):
     return time.perf_counter() - t0
 
 
+def host_sample(w, nb, B, seed=0):
+    """K and V for nb blocks of one layer, drawn on the host with the
+    workload's value distribution and rounded to its source dtype."""
+    from oracle.numerics import round_to
+    r = np.random.default_rng(seed)
+    shape = (1, nb, B, w.H, w.d)
+    dist = w.extra.get("dist", ("normal", 1.0))
+
+    def draw():
+        if dist[0] == "student_t":
+            x = r.standard_t(dist[1], shape) * dist[2]
+        else:
+            x = r.standard_normal(shape) * dist[1]
+            if dist[0] == "normal_outliers":        # dist[2] channels per head, times dist[3]
+                for h in range(w.H):
+                    x[..., h, r.choice(w.d, size=dist[2], replace=False)] *= dist[3]
+        return round_to(x, w.src_dtype)
+    return draw(), draw()
+
+
+def cpu_baseline_workload(w, blk, wire, budget_s=15.0):
+    """The oracle on a bounded sample of a per-layer workload: one layer, the
+    first blocks of one block size (as many as fit the budget), with the
+    workload's wire, encode + table + fetch."""
+    import copy
+    w1 = copy.copy(w)
+    w1.L = 1
+
+    def sub(nb):
+        ids = np.arange(nb, dtype=np.int32)
+        return type(blk)(blk.B, ids, ids.copy(), blk.n_valid[:nb].copy(), blk.delta_m[:nb].copy(),
+                         nb, nb)
+    nb = 8
+    k, v = host_sample(w1, nb, blk.B)
+    t = oracle_small(w1, sub(nb), k, v, wire)        # calibrate
+    nb = int(min(blk.nb, max(8, nb * budget_s / max(t, 1e-3) / 1.1)))
+    s = sub(nb)
+    k, v = host_sample(w1, nb, blk.B)
+    t = oracle_small(w1, s, k, v, wire)
+    b = sum(small_bytes(w1, s, wire).values())
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 of {w.L} layers x {nb} of {blk.nb} blocks of {blk.B} tokens "
+                      f"({s.tokens()} tokens) of {w.name}, {wire} encode + table + fetch, "
+                      f"float64 numpy, one thread; {t:.1f} s",
+            "tokens_per_s": s.tokens() / t}
+
+
 def run_small(args):
     """The small workloads (tiny, gqa_reorder): every wire's encode + table +
     fetch over all layers, with L2 flushed before every timed pass (their
@@ -918,6 +965,8 @@ def run_layered(args):
                             "call's span includes time shared with other calls; the pass's rate "
                             "is `value`, its time per layer `per_layer_us`"},
         "per_layer_us": total_s / args.steps / w.L * 1e6,
+        "cpu_baseline": (cpu_baseline_workload(w, w.blocks[0], wire, args.cpu_seconds)
+                         if "cpu" in args.legs and rank == 0 else None),
         "peak": peak, "peak_source": peak_kind, "gpu_launches": 2 * n_calls,
         "clocks": clocks.summary()}))
 

@@ -33,3 +33,13 @@ def test_parallel_oracle_leg_reports_a_failing_worker():
     w.src_dtype = "no-such-dtype"
     r = bench.cpu_baseline_parallel(w, w.blocks[0], nb=4, procs=2)
     assert "unavailable" in r and "value" not in r, r
+
+
+def test_oracle_leg_of_the_per_layer_workloads():
+    """The layered lines' oracle leg: one layer, the first blocks of one block
+    size, the workload's wire and value distribution."""
+    for name, wire in (("ragged", "int4"), ("llama3_70b", "fp8")):
+        w = workloads.WORKLOADS[name]()
+        r = bench.cpu_baseline_workload(w, w.blocks[0], wire, budget_s=0.3)
+        assert r["kind"] == "oracle" and r["cores"] == 1 and r["unit"] == "GB/s"
+        assert r["value"] > 0 and r["tokens_per_s"] > 0 and f"of {name}, {wire}" in r["sample"]
