@@ -326,3 +326,15 @@ def test_exact_ties_16bit(fmt):
     _assert_ok(parity.run_case(c, "int4", scale_dtype="f32"))
     _assert_ok(parity.run_case(c, "fp8_rows", scale_dtype="f16"))
     _assert_ok(parity.run_case(c, "fp8_rows", scale_dtype="f32"))
+
+
+@pytest.mark.parametrize("wire", ["fp8", "raw"])
+@pytest.mark.parametrize("pairing", ["half_split", "interleaved"])
+def test_extreme_delta_m(wire, pairing):
+    """Delta-m at the ends of its int32 range: the table's fp64 angles reach
+    2^31 rad (large-argument reduction in both the kernel's sincos and the
+    oracle's), and the rotated keys still meet the bars."""
+    c = parity.random_case(4242, L=1, H=2, d=128, B=16, nb=7, src_fmt="f32", out_fmt="f32",
+                           pairing=pairing)
+    c.delta_m = np.array([0, 1, -1, 1 << 30, -(1 << 30), (1 << 31) - 1, -(1 << 31)], np.int64)
+    _assert_ok(parity.run_case(c, wire))
