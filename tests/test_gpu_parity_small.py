@@ -338,3 +338,15 @@ def test_extreme_delta_m(wire, pairing):
                            pairing=pairing)
     c.delta_m = np.array([0, 1, -1, 1 << 30, -(1 << 30), (1 << 31) - 1, -(1 << 31)], np.int64)
     _assert_ok(parity.run_case(c, wire))
+
+
+@pytest.mark.parametrize("wire", ["fp8", "int4", "fp8_rows"])
+def test_shared_source_slots_and_single_rows(wire):
+    """Several blocks gathered from the same source slot (only destinations
+    must be distinct), every block valid for a single row: the amax, the
+    scale and the codes come from that row alone."""
+    c = parity.random_case(515, L=2, H=3, d=128, B=16, nb=6, src_fmt="bf16", out_fmt="bf16",
+                           pairing="half_split")
+    c.src_slots = np.array([2, 2, 5, 2, 5, 0], np.int32)
+    c.n_valid = np.ones(6, np.int32)
+    _assert_ok(parity.run_case(c, wire))
