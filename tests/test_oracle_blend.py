@@ -44,4 +44,3 @@ def test_ties_go_to_the_lower_index():
     assert np.array_equal(blend.select_topk(v, 4), [1, 2, 3, 4])
     assert np.array_equal(blend.select_topk(v, 5), [1, 2, 3, 4, 6])
     assert np.array_equal(blend.select_topk(v, 7), np.arange(7))
-
