@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define HC_API_VERSION 2
+#define HC_API_VERSION 3
 
 typedef enum hc_status {
   HC_OK = 0,
@@ -256,10 +256,11 @@ int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, in
  *   drift[s][t] = sqrt( sum_c (h_fresh[s][t][c] - h_cached[s][t][c])^2 )
  * (differences, squares and the sum in fp32; the sum's order is the
  * library's), and selected[s][0..k) = the k tokens with the largest drift,
- * ties to the lower index, in ascending order.  The caller picks k; about 15%
- * of the tokens is the page's figure.
- * [HyperCache page, "Core Design", selective recomputation ("top ~15% of
- *  tokens with the largest Layer-0 hidden-state drift", CacheBlend).]
+ * ties to the lower index, in ascending order.  The caller picks k, or
+ * passes k <= 0 for the page's share, hc_selection_size(n_tokens).
+ * [HyperCache page, "Core Design", selective recomputation: about 15% of the
+ *  tokens, those whose layer-0 hidden state moved furthest, are recomputed,
+ *  as in CacheBlend.]
  *
  *   h_cached, h_fresh : device, dtype f32/f16/bf16, 16-byte aligned; element
  *                       (s, t, c) at base + s*seq_stride + t*token_stride + c
@@ -269,13 +270,22 @@ int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, in
  *   token_stride : >= hidden; seq_stride >= n_tokens * token_stride when
  *                  n_seq > 1; both in elements, times the element size a
  *                  multiple of 16 bytes
- *   k            : 1 <= k <= n_tokens
+ *   k            : 1 <= k <= n_tokens, or <= 0 for hc_selection_size(n_tokens)
  *   drift        : device f32 [n_seq][n_tokens], written in full
- *   selected     : device int32 [n_seq][k], written in full
+ *   selected     : device int32 [n_seq][k] (k after the default is applied),
+ *                  written in full
  * Hidden states must be finite.  Returns HC_OK, HC_ERR_INVALID_ARG or HC_ERR_CUDA. */
 int hc_drift_select(const void* h_cached, const void* h_fresh, int32_t dtype, int32_t n_seq,
                     int32_t n_tokens, int32_t hidden, int64_t token_stride, int64_t seq_stride,
                     int32_t k, float* drift, int32_t* selected, void* stream);
+
+/* hc_selection_size: the number of tokens per sequence that hc_drift_select
+ * recomputes by default: ceil(15% of n_tokens), computed exactly in integers
+ * as ceil(3 * n_tokens / 20); 1 or more for n_tokens >= 1, 0 for
+ * n_tokens <= 0.  A host function (nothing runs on the GPU).
+ * [HyperCache page, "Core Design", selective recomputation: about 15% of the
+ *  tokens are recomputed.] */
+int32_t hc_selection_size(int32_t n_tokens);
 
 /* Block digests for cache lookup (host functions: every pointer is a host
  * pointer; nothing runs on the GPU).  Two deterministic 128-bit BLAKE2b

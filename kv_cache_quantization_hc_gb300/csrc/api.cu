@@ -288,12 +288,20 @@ int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, in
   return record(hc::launch_crc32(p, static_cast<cudaStream_t>(stream)));
 }
 
+int32_t hc_selection_size(int32_t n_tokens) {
+  // ceil(15% of n_tokens) in integers: 15/100 = 3/20; n_tokens < 2^31 keeps
+  // 3 * n_tokens + 19 inside int64.
+  if (n_tokens < 1) return 0;
+  return static_cast<int32_t>((int64_t{3} * n_tokens + 19) / 20);
+}
+
 int hc_drift_select(const void* h_cached, const void* h_fresh, int32_t dtype, int32_t n_seq,
                     int32_t n_tokens, int32_t hidden, int64_t token_stride, int64_t seq_stride,
                     int32_t k, float* drift, int32_t* selected, void* stream) {
   const int es = elem_size(dtype);
   if (es == 0 || n_seq < 0 || n_tokens < 1 || hidden < 8 || hidden % 8) return HC_ERR_INVALID_ARG;
-  if (k < 1 || k > n_tokens) return HC_ERR_INVALID_ARG;
+  if (k <= 0) k = hc_selection_size(n_tokens);
+  if (k > n_tokens) return HC_ERR_INVALID_ARG;
   if (!h_cached || !h_fresh || !drift || !selected) return HC_ERR_INVALID_ARG;
   if (token_stride < hidden || (n_seq > 1 && seq_stride < int64_t{n_tokens} * token_stride))
     return HC_ERR_INVALID_ARG;

@@ -113,8 +113,10 @@ __device__ __forceinline__ void fp8x8_to_float2(uint2 c, float s, float2 (&x)[4]
 // 8 nibbles -> 8 floats code * s.  Biasing every nibble by 8 makes it the
 // unsigned value code + 8 in [1, 15]; placed in the low byte of the fp32
 // pattern of 2^23 it reads as 2^23 + code + 8, so one subtraction of 2^23 + 8
-// gives the code exactly, and one multiply by s the exact product (|code| <= 7
-// times a scale of at most 24 significant bits).
+// gives the code exactly, and one multiply by s gives code * s with one
+// correct fp32 rounding, the value the oracle computes.  With an fp16 scale
+// (11 significant bits) the product needs at most 14 bits and is exact; an
+// fp32 scale can need 27, and then the multiply rounds it once.
 __device__ __forceinline__ void int4x8_to_float2(uint32_t c, float s, float2 (&x)[4]) {
   const uint32_t b = c ^ 0x88888888u;
   const uint32_t even = b & 0x0f0f0f0fu;         // byte i: element 2i

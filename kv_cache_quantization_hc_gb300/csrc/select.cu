@@ -3,8 +3,9 @@
 // layer-0 KV is exact; the tokens whose layer-0 hidden state drifted most are
 // recomputed through the deeper layers.
 // ["HyperCache - Distributed KV-cache quantization and relative RoPE reuse",
-//  "Core Design", selective recomputation ("top ~15% of tokens with the
-//  largest Layer-0 hidden-state drift", following CacheBlend).]
+//  "Core Design", selective recomputation: about 15% of the tokens, those
+//  whose layer-0 hidden state moved furthest, are recomputed, as in
+//  CacheBlend.]
 //
 //   drift[s][t]  = fp32 sqrt( sum_c (fresh - cached)^2 ), summed in fp32;
 //   selected[s]  = the k tokens of sequence s with the largest drift (ties to
@@ -52,7 +53,8 @@ __global__ void __launch_bounds__(kThreads) k_drift(SelectParams p) {
 constexpr int kSelectThreads = 1024;
 
 // Exclusive prefix count of `flag` over the CTA (in thread order) and the
-// total; `warp_sums` holds 32 words of shared memory.
+// total; `warp_sums` holds 33 words of shared memory (32 warp counts, then
+// the CTA's total).
 __device__ __forceinline__ int block_scan(bool flag, uint32_t* warp_sums, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t ballot = __ballot_sync(0xffffffffu, flag);

@@ -72,6 +72,8 @@ def lib():
         L.hc_last_cuda_error.restype = ctypes.c_char_p
         L.hc_version.argtypes = []
         L.hc_version.restype = ctypes.c_int32
+        L.hc_selection_size.argtypes = [_I32]
+        L.hc_selection_size.restype = ctypes.c_int32
         _LIB = L
     return _LIB
 
@@ -260,33 +262,38 @@ def hc_crc32(a, a_bytes, a_stride, b, b_bytes, b_stride, n_units, crc, stream=No
 
 def hc_drift_select(h_cached, h_fresh, dtype, n_seq, n_tokens, hidden, token_stride, seq_stride, k,
                     drift, selected, stream=None):
-    if (n_seq > 0 and n_tokens > 0 and hidden > 0 and dtype in _ES and 0 < k <= n_tokens
+    # k <= 0 asks the library for its default; the size check below needs the
+    # k the library will use, which it reports through hc_selection_size
+    k_used = hc_selection_size(n_tokens) if k <= 0 else k
+    if (n_seq > 0 and n_tokens > 0 and hidden > 0 and dtype in _ES and 0 < k_used <= n_tokens
             and token_stride >= hidden and seq_stride >= n_tokens * token_stride):
         es = _ES[dtype]
         span = ((n_seq - 1) * seq_stride + (n_tokens - 1) * token_stride + hidden) * es
         _need(h_cached, span, "h_cached")
         _need(h_fresh, span, "h_fresh")
         _need(drift, 4 * n_seq * n_tokens, "drift")
-        _need(selected, 4 * n_seq * k, "selected")
+        _need(selected, 4 * n_seq * k_used, "selected")
     _check("hc_drift_select", lib().hc_drift_select(
         _dptr(h_cached, "h_cached"), _dptr(h_fresh, "h_fresh"), dtype, n_seq, n_tokens, hidden,
         token_stride, seq_stride, k, _dptr(drift, "drift"), _dptr(selected, "selected"),
         _stream(stream)))
 
 
-def selection_size(n_tokens, fraction=0.15):
-    """Tokens a sequence recomputes: ceil(fraction * n_tokens), at least 1,
-    with the fraction taken exactly as the decimal it is written as (0.15 of
-    100 tokens is 15, not 16)."""
-    from fractions import Fraction
-    f = Fraction(str(fraction))
-    return max(1, -((-f.numerator * int(n_tokens)) // f.denominator))
+def hc_selection_size(n_tokens):
+    return lib().hc_selection_size(n_tokens)
+
+
+def selection_size(n_tokens):
+    """The library's default number of tokens to recompute per sequence
+    (hc_selection_size)."""
+    return hc_selection_size(int(n_tokens))
 
 
 def drift_select(h_cached, h_fresh, k=None, drift=None, selected=None, stream=None):
     """hc_drift_select on tensors shaped [n_seq, n_tokens, hidden] (or
     [n_tokens, hidden]); returns (drift [n_seq, n_tokens] f32, selected
-    [n_seq, k] int32).  k defaults to selection_size(n_tokens)."""
+    [n_seq, k] int32).  k = None takes the library's default,
+    hc_selection_size(n_tokens)."""
     import torch
     if h_cached.dim() == 2:
         h_cached, h_fresh = h_cached.unsqueeze(0), h_fresh.unsqueeze(0)

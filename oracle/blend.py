@@ -4,11 +4,11 @@ ORACLE (test infrastructure only; see the package docstring).
 
 The page pairs the relative RoPE rotation with selective recomputation: layer
 0 K/V depends only on the token embeddings, so the rotated layer-0 KV is
-exact, and "the top ~15% of tokens with the largest Layer-0 hidden-state
-drift are selectively recomputed through deeper layers (following the
-CacheBlend approach)" ["HyperCache - Distributed KV-cache quantization and
-relative RoPE reuse", "Core Design", paragraph after the relative-RoPE
-identity; "Example output" part A, "RoPE Shift + 15% CacheBlend"].
+exact, and about 15% of the tokens, those whose layer-0 hidden state moved
+furthest, are recomputed through the deeper layers, following CacheBlend
+["HyperCache - Distributed KV-cache quantization and relative RoPE reuse",
+"Core Design", paragraph after the relative-RoPE identity; "Example output"
+part A, "RoPE Shift + 15% CacheBlend"].
 
 Reading taken (the page gives no formula):
 

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     from kv_cache_quantization_hc_gb300 import hc
-    assert hc.hc_version() == 2
+    assert hc.hc_version() == 3
     assert hc.status_string(0) == "HC_OK"
     assert hc.status_string(-1) == "HC_ERR_INVALID_ARG"
     assert hc.status_string(-2) == "HC_ERR_UNSUPPORTED"
@@ -123,7 +123,8 @@ def test_host_validation_of_drift_select(lib):
     ok = (A, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 15, A, A, None)
     assert d(*ok[:2], 9, *ok[3:]) == hc.HC_ERR_INVALID_ARG                       # dtype
     assert d(A, A, hc.HC_BF16, 2, 100, 60, 64, 6400, 15, A, A, None) == hc.HC_ERR_INVALID_ARG   # hidden % 8
-    assert d(A, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 0, A, A, None) == hc.HC_ERR_INVALID_ARG    # k = 0
+    # k <= 0 takes the default (15 of 100 tokens): valid, so an invalid stride still decides
+    assert d(A, A, hc.HC_BF16, 2, 100, 64, 60, 6400, 0, A, A, None) == hc.HC_ERR_INVALID_ARG    # stride
     assert d(A, A, hc.HC_BF16, 2, 100, 64, 64, 6400, 101, A, A, None) == hc.HC_ERR_INVALID_ARG  # k > T
     assert d(A, A, hc.HC_BF16, 2, 100, 64, 60, 6400, 15, A, A, None) == hc.HC_ERR_INVALID_ARG   # stride
     assert d(A, A, hc.HC_BF16, 2, 100, 64, 64, 6000, 15, A, A, None) == hc.HC_ERR_INVALID_ARG   # overlap

@@ -117,3 +117,22 @@ def test_full_size_workload_sampled():
     for seq in (0, 31, 63):
         c1, f1 = workloads.blend_hidden(w, DEV, seqs=[seq])
         _check(c1, f1, k, d[seq:seq + 1], s[seq:seq + 1])
+
+
+def test_default_k_through_the_c_abi():
+    """k = 0 through the C ABI selects the library's default share of the
+    tokens (hc_selection_size): the oracle's ceil(15%), and the same drift and
+    selection as an explicit k of that size."""
+    from kv_cache_quantization_hc_gb300 import hc
+    w = workloads.blend_small()
+    cached, fresh = workloads.blend_hidden(w, DEV)
+    k = blend.default_k(w.n_tokens)
+    assert hc.lib().hc_selection_size(w.n_tokens) == k
+    n_seq, T, D = cached.shape
+    drift = torch.empty((n_seq, T), dtype=torch.float32, device=DEV)
+    sel = torch.full((n_seq, k), -1, dtype=torch.int32, device=DEV)
+    hc.hc_drift_select(cached, fresh, hc.HC_BF16, n_seq, T, D, D, T * D, 0, drift, sel)
+    d2, s2 = hc.drift_select(cached, fresh, k)
+    torch.cuda.synchronize()
+    assert torch.equal(drift, d2) and torch.equal(sel, s2)
+    _check(cached, fresh, k, drift, sel)

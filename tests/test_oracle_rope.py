@@ -1,11 +1,11 @@
 """Pins for the oracle's RoPE, strip-RoPE and relative rotation (CPU only):
 closed forms, the SO(2) identity, composition, inversion, norm preservation,
-complex multiplication for d = 2, and the pages' printed fp32 error."""
+and the 2x2 rotation matrix for d = 2.  The pages' printed fp32 shift error is
+pinned through the oracle's rotation table in test_oracle_table.py."""
 import numpy as np
 import pytest
 
 from oracle import rope
-from oracle.numerics import round_to
 
 PAIRINGS = [rope.INTERLEAVED, rope.HALF_SPLIT]
 
@@ -41,13 +41,21 @@ def test_unit_vector_closed_form(pairing):
         assert np.allclose(y, want, atol=1e-15)
 
 
-def test_d2_matches_complex_multiplication():
+def test_d2_matches_rotation_matrix():
+    """d = 2 (theta_0 = 1): each token's pair is the 2x2 rotation matrix
+    [[cos m, -sin m], [sin m, cos m]] times the column (x0, x1), multiplied
+    out by numpy's matmul."""
     rng = np.random.default_rng(0)
     x = rng.standard_normal((50, 3, 2))
-    pos = rng.integers(-5000, 5000, 50)
+    pos = rng.integers(-5000, 5000, 50).astype(float)
     y = rope.apply_rope(x, pos, rope.inv_freq(2, 1e4), rope.INTERLEAVED)
-    z = (x[..., 0] + 1j * x[..., 1]) * np.exp(1j * pos.astype(float))[:, None]
-    assert np.allclose(y[..., 0], z.real, atol=1e-12) and np.allclose(y[..., 1], z.imag, atol=1e-12)
+    c, s = np.cos(pos), np.sin(pos)
+    R = np.stack([np.stack([c, -s], -1), np.stack([s, c], -1)], -2)      # [T, 2, 2]
+    want = np.matmul(R[:, None], x[..., None])[..., 0]                  # [T, 3, 2]
+    assert np.allclose(y, want, atol=1e-12, rtol=0)
+    back = rope.strip_rope(y, pos, rope.inv_freq(2, 1e4), rope.INTERLEAVED)
+    assert np.allclose(back, np.matmul(np.swapaxes(R, 1, 2)[:, None], y[..., None])[..., 0],
+                       atol=1e-12, rtol=0)
 
 
 @pytest.mark.parametrize("pairing", PAIRINGS)
@@ -89,24 +97,3 @@ def test_composition_and_inverse_and_norm(pairing):
     a, b = rope.pair_channels(d, pairing)
     y = rope.apply_rope(x, pos, th, pairing)
     assert np.allclose(x[..., a] ** 2 + x[..., b] ** 2, y[..., a] ** 2 + y[..., b] ** 2, rtol=1e-12)
-
-
-def test_pages_fp32_shift_error(golden):
-    """Moving fp32 post-RoPE keys from position 1024 to 8192 with an fp32
-    rotation lands within 1e-6 of fresh RoPE at 8192; the pages print 4.77e-7."""
-    rng = np.random.default_rng(4)
-    d, base = 128, 1e4
-    th = rope.inv_freq(d, base)
-    x = rng.standard_normal((256, 8, d))
-    a, b = rope.pair_channels(d, rope.INTERLEAVED)
-    k_old = round_to(rope.apply_rope(x, np.full(256, 1024), th, rope.INTERLEAVED), "f32").astype(np.float32)
-    ang = 7168 * th
-    c = round_to(np.cos(ang), "f32").astype(np.float32)
-    s = round_to(np.sin(ang), "f32").astype(np.float32)
-    y = np.empty_like(k_old)
-    y[..., a] = k_old[..., a] * c - k_old[..., b] * s
-    y[..., b] = k_old[..., a] * s + k_old[..., b] * c
-    ref = rope.apply_rope(x, np.full(256, 8192), th, rope.INTERLEAVED)
-    err = np.max(np.abs(y.astype(np.float64) - ref))
-    assert err <= 1e-6
-    assert err >= golden["rope_shift_err_1024_to_8192"] / 8     # same order as printed
