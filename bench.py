@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "KV fetch+rotate+scatter GB/s and tokens/s; % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = {
     "k_encode": ["encode.cu", "encode_common.cuh", "crc_math.h", "hc_internal.cuh", "fastdiv.h"],
     "k_fetch": ["fetch_impl.cuh", "fetch_fp8.cu", "hc_internal.cuh", "fastdiv.h"],
@@ -90,25 +91,29 @@ def kernel_source_hash(kernel):
 
 
 def profiled_traffic(kernel, workload):
-    """DRAM bytes per launch recorded by ncu in profiles/, if the kernel's
-    sources are unchanged since; else None."""
+    """DRAM traffic of one launch recorded by ncu in profiles/ (a capture of
+    the full-size launch), if the kernel's sources are unchanged since; else
+    None.  Returns {"traffic", "read", "write", "capture"}."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         with open(path) as f:
             text = f.read()
     except OSError:
         return None
+    keys = ("dram_read_bytes_per_launch", "dram_write_bytes_per_launch", "source_sha256", "capture")
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
+        if ":" in line and line.strip().startswith(keys):
             k, v = line.split(":", 1)
             vals[k.strip().strip("-* `")] = v.strip().strip("`")
     if vals.get("source_sha256") != kernel_source_hash(kernel):
         return None
     try:
-        return int(vals["traffic_bytes_per_launch"])
+        rd, wr = int(vals["dram_read_bytes_per_launch"]), int(vals["dram_write_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+    return {"traffic": rd + wr, "read": rd, "write": wr, "capture": vals.get("capture"),
+            "source": f"profiles/{kernel}_{workload}.md"}
 
 
 class ClockSampler:
@@ -280,7 +285,7 @@ def run_ours(args):
     kname = {"encode": "k_encode", "fetch": "k_fetch"}[dominant]
     if args.codec == "fp8_rows":
         kname += "_fp8_rows"
-    traffic = profiled_traffic(kname, "qwen3_8b") if not args.layers else None
+    prof = profiled_traffic(kname, "qwen3_8b") if not args.layers else None
     achieved = kern[dominant]["gbs"]
 
     crc = run_crc(args, p, device, src_k, src_v) if args.crc else None
@@ -288,6 +293,13 @@ def run_ours(args):
     if "e2e" in args.legs:
         e2e = run_e2e(args, w, blk, p, src_k, src_v, dst_k, dst_v, step_bytes, device,
                       device_step_s=total_s / args.steps)
+    wl = None
+    if "workloads" in args.legs and not args.layers:
+        del p, src_k, src_v, dst_k, dst_v
+        torch.cuda.empty_cache()
+        with ClockSampler(local) as wl_clocks:
+            wl = workload_lines(args, device)
+        wl["clocks"] = wl_clocks.summary()
     cpu = None
     if "cpu" in args.legs and rank == 0 and world == 1:
         cpu = cpu_baseline(w, blk, budget_s=args.cpu_seconds)
@@ -316,9 +328,14 @@ def run_ours(args):
             "hbm_frac": total_bytes / max_s / 1e9 / world / peak,
             "kernels": kern,
             "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
-                         "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None if prof is None else prof["traffic"],
+                         "traffic_detail": prof,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, a 1:1 copy)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                         "nominal_peak": f"{NOMINAL_HBM_GBS:.0f} GB/s, the nominal ~8 TB/s HBM3e "
+                                         f"figure (frac is against the measured copy peak)",
                          "algorithmic_bytes_per_launch": nbytes[dominant]},
             "gpu_launches": 3 * args.steps,
             "clocks": clocks.summary(),
@@ -327,6 +344,8 @@ def run_ours(args):
         }
         if crc is not None:
             line["crc32"] = crc
+        if wl is not None:
+            line["workloads"] = wl
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -853,18 +872,164 @@ def layered_bytes(w, blk, wire, group=32):
     return enc, fet
 
 
+def fetch_target_us(fetch_bytes, frac=0.7, nominal_gbs=8000.0):
+    """Time a fetch call may take at `frac` of the nominal ~8 TB/s HBM peak."""
+    return fetch_bytes / (frac * nominal_gbs * 1e9) * 1e6
+
+
+def measure_layered(w, wire, device, steps, warmup, K=2, distinct_layers=False):
+    """Per-layer calls of a workload (one call per layer and block size), in
+    three timed passes over all layers:
+
+    * encode alone: the encodes back to back on one stream, each call between
+      CUDA events on that stream;
+    * fetch alone: the fetches back to back on a side stream, each timed;
+    * layered: layer l encoded on encode stream l % K and then fetched on
+      fetch stream l % K after an event, so neighbouring layers overlap (the
+      layer-streamed schedule); timed as a whole.
+
+    With `distinct_layers`, every layer has its own wire and its own slice of
+    an all-layer destination cache (the layer-streamed fetch into one paged
+    cache); otherwise each block size keeps a ring of 2K wire buffers
+    (layer l encodes into slot l % 2K only after the fetch that last read it
+    has finished) and each fetch stream writes its own destination pool.  The
+    sources are two drawn layers per block size, used alternately (each is
+    larger than L2)."""
+    import torch
+    import workloads
+    from kv_cache_quantization_hc_gb300 import path as kvpath
+
+    K = max(1, K)
+    R = w.L if distinct_layers else 2 * K
+    main = torch.cuda.current_stream(device)
+    enc_streams = [main] + [torch.cuda.Stream(device=device) for _ in range(K - 1)]
+    fet_streams = [torch.cuda.Stream(device=device) for _ in range(K)]
+    odt = workloads.torch_dtype(w.out_dtype)
+    groups = []
+    for blk in w.blocks:
+        p = kvpath.from_blocks(w, blk, wire, device=device, n_layers=R, scale_dtype="f16")
+        srcs = [(workloads.device_pool(w, blk, range(i, i + 1), 0, device),
+                 workloads.device_pool(w, blk, range(i, i + 1), 1, device)) for i in range(2)]
+        n_dst = w.L if distinct_layers else K
+        shape = (n_dst, blk.num_dst_slots, blk.B, w.H, w.d)
+        dst = (torch.empty(shape, dtype=odt, device=device), torch.empty(shape, dtype=odt, device=device))
+        p.build_table(stream=main)
+        groups.append(dict(blk=blk, p=p, srcs=srcs, dst=dst, bytes=layered_bytes(w, blk, wire)))
+
+    def wire_of(g, layer):
+        i = layer % R
+        return g["p"].codes[i:i + 1], g["p"].scales[i:i + 1]
+
+    def dst_of(g, layer, fs_index):
+        i = layer if distinct_layers else fs_index
+        return g["dst"][0][i:i + 1], g["dst"][1][i:i + 1]
+
+    def encode_pass(rec):
+        for layer in range(w.L):
+            for gi, g in enumerate(groups):
+                codes, scales = wire_of(g, layer)
+                sk, sv = g["srcs"][layer % 2]
+                if rec: rec[layer][gi][0].record(main)
+                g["p"].encode(sk, sv, stream=main, codes=codes, scales=scales)
+                if rec: rec[layer][gi][1].record(main)
+
+    def fetch_pass(rec):
+        fs = fet_streams[0]
+        fs.wait_stream(main)
+        for layer in range(w.L):
+            for gi, g in enumerate(groups):
+                codes, scales = wire_of(g, layer)
+                dk, dv = dst_of(g, layer, 0)
+                if rec: rec[layer][gi][0].record(fs)
+                g["p"].fetch(dk, dv, stream=fs, codes=codes, scales=scales)
+                if rec: rec[layer][gi][1].record(fs)
+        main.wait_stream(fs)
+
+    def layered_pass():
+        for st in enc_streams[1:] + fet_streams:
+            st.wait_stream(main)
+        fetched = {}
+        for layer in range(w.L):
+            es, fs = enc_streams[layer % K], fet_streams[layer % K]
+            for gi, g in enumerate(groups):
+                codes, scales = wire_of(g, layer)
+                if layer >= R:                       # the slot's previous reader is done
+                    es.wait_event(fetched[(layer - R, gi)])
+                sk, sv = g["srcs"][layer % 2]
+                g["p"].encode(sk, sv, stream=es, codes=codes, scales=scales)
+                done = torch.cuda.Event()
+                done.record(es)
+                fs.wait_event(done)
+                dk, dv = dst_of(g, layer, layer % K)
+                g["p"].fetch(dk, dv, stream=fs, codes=codes, scales=scales)
+                fetched[(layer, gi)] = torch.cuda.Event()
+                fetched[(layer, gi)].record(fs)
+        for st in enc_streams[1:] + fet_streams:
+            main.wait_stream(st)
+
+    def call_events():
+        return [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in groups]
+                for _ in range(w.L)]
+
+    for _ in range(warmup):
+        encode_pass(None)
+        fetch_pass(None)
+        layered_pass()
+    torch.cuda.synchronize(device)
+    enc_rec = [call_events() for _ in range(steps)]
+    fet_rec = [call_events() for _ in range(steps)]
+    for i in range(steps):
+        encode_pass(enc_rec[i])
+    for i in range(steps):
+        fetch_pass(fet_rec[i])
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(main)
+    for _ in range(steps):
+        layered_pass()
+    end.record(main)
+    torch.cuda.synchronize(device)
+    if any(g["p"].error_bits() for g in groups):
+        raise RuntimeError("device error flag set")
+    pass_s = start.elapsed_time(end) / 1e3 / steps
+    peak, _ = measured_peaks()
+    per_kernel = {}
+    for name, recs, bi in (("encode", enc_rec, 0), ("fetch", fet_rec, 1)):
+        per_kernel[name] = {}
+        for gi, g in enumerate(groups):
+            ts = [r[layer][gi][0].elapsed_time(r[layer][gi][1]) / 1e3 for r in recs for layer in range(w.L)]
+            med = statistics.median(ts)
+            b = g["bytes"][bi]
+            per_kernel[name][f"B{g['blk'].B}"] = {
+                "median_us": med * 1e6, "min_us": min(ts) * 1e6, "calls": len(ts),
+                "bytes_per_call": b, "gbs": b / med / 1e9, "frac": b / med / 1e9 / peak,
+                "tokens_per_s": g["blk"].tokens() / med}
+    pass_bytes = sum(g["bytes"][0] + g["bytes"][1] for g in groups) * w.L
+    tokens = sum(g["blk"].tokens() for g in groups)
+    out = {"layers": w.L, "tokens": tokens, "wire": wire,
+           "blocks": "/".join(f"{g['blk'].nb}xB{g['blk'].B}" for g in groups),
+           "encode": per_kernel["encode"], "fetch": per_kernel["fetch"],
+           "pass": {"gbs": pass_bytes / pass_s / 1e9, "frac": pass_bytes / pass_s / 1e9 / peak,
+                    "ms_per_pass": pass_s * 1e3, "per_layer_us": pass_s / w.L * 1e6,
+                    "tokens_per_s": tokens / pass_s, "bytes_per_pass": pass_bytes,
+                    "schedule": f"layer l: encode on stream l % {K}, then fetch on fetch stream "
+                                f"l % {K} after an event"},
+           "timing": f"CUDA events on the launching stream, {steps} passes after {warmup} warm-up "
+                     "passes; per-call figures from the passes of that kernel alone",
+           "buffers": ("one wire and one destination-cache slice per layer" if distinct_layers else
+                       f"wire ring of {R} per block size, {K} destination pools"),
+           "peak_gbs": peak}
+    for g in groups:
+        del g["p"], g["srcs"], g["dst"]
+    return out
+
+
 def run_layered(args):
-    """Per-layer calls: every layer is encoded on an encode stream and then
-    fetched on a fetch stream (after an event), as a layer-streamed fetch runs.
-    With --layer-streams K, layer l uses encode stream l % K and fetch stream
-    l % K, so neighbouring layers' calls may overlap. Each block size keeps a
-    ring of 2K wire buffers: layer l encodes into slot l % 2K only after the
-    fetch that last read that slot has finished. Each fetch stream writes its
-    own destination pool."""
+    """The per-layer workloads on their own (llama3_70b: FP8, one wire and
+    destination slice per layer; ragged: --wire, rings), one JSON line."""
     import torch
     import __graft_entry__
     import workloads
-    from kv_cache_quantization_hc_gb300 import path as kvpath
 
     rank, world, local = dist_env()
     device = torch.device("cuda", local)
@@ -874,101 +1039,45 @@ def run_layered(args):
     if args.layers:
         w.L = args.layers
     wire = "fp8" if args.workload == "llama3_70b" else args.wire
-    K = max(1, args.layer_streams)
-    R = 2 * K
-    main = torch.cuda.current_stream(device)
-    enc_streams = [main] + [torch.cuda.Stream(device=device) for _ in range(K - 1)]
-    fet_streams = [torch.cuda.Stream(device=device) for _ in range(K)]
-    groups = []
-    for blk in w.blocks:
-        p = kvpath.from_blocks(w, blk, wire, device=device, n_layers=1, scale_dtype="f16")
-        src_k = workloads.device_pool(w, blk, range(0, 1), 0, device)
-        src_v = workloads.device_pool(w, blk, range(0, 1), 1, device)
-        shape = (1, blk.num_dst_slots, blk.B, w.H, w.d)
-        dst = [(torch.empty(shape, dtype=workloads.torch_dtype(w.out_dtype), device=device),
-                torch.empty(shape, dtype=workloads.torch_dtype(w.out_dtype), device=device))
-               for _ in range(K)]
-        ring = [(torch.empty_like(p.codes), None if p.scales is None else torch.empty_like(p.scales))
-                for _ in range(R)]
-        p.build_table(stream=main)
-        groups.append((blk, p, src_k, src_v, dst, ring, layered_bytes(w, blk, wire)))
-
-    def step(record):
-        for st in enc_streams[1:] + fet_streams:
-            st.wait_stream(main)
-        fetched = {}
-        for layer in range(w.L):
-            es, fs = enc_streams[layer % K], fet_streams[layer % K]
-            for gi, (blk, p, sk, sv, dst, ring, _) in enumerate(groups):
-                e = record[layer][gi] if record else None
-                codes, scales = ring[layer % R]
-                if layer >= R:                       # the slot's previous reader is done
-                    es.wait_event(fetched[(layer - R, gi)])
-                if e: e[0].record(es)
-                p.encode(sk, sv, stream=es, codes=codes, scales=scales)
-                if e: e[1].record(es)
-                done = torch.cuda.Event()
-                done.record(es)
-                fs.wait_event(done)
-                dk, dv = dst[layer % K]
-                if e: e[2].record(fs)
-                p.fetch(dk, dv, stream=fs, codes=codes, scales=scales)
-                if e: e[3].record(fs)
-                fetched[(layer, gi)] = torch.cuda.Event()
-                fetched[(layer, gi)].record(fs)
-        for st in enc_streams[1:] + fet_streams:
-            main.wait_stream(st)
-
-    for _ in range(args.warmup):
-        step(None)
-    torch.cuda.synchronize(device)
-    rec = [[[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in groups]
-            for _ in range(w.L)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
-        torch.cuda.synchronize(device)
-        start.record(main)
-        for i in range(args.steps):
-            step(rec[i])
-        end.record(main)
-        torch.cuda.synchronize(device)
-    total_s = start.elapsed_time(end) / 1e3
-    if any(g[1].error_bits() for g in groups):
-        raise RuntimeError("device error flag set")
-    enc_t, fet_t = [], []
-    for r in rec:
-        for layer in r:
-            for e in layer:
-                enc_t.append(e[0].elapsed_time(e[1]) / 1e3)
-                fet_t.append(e[2].elapsed_time(e[3]) / 1e3)
-    enc_b = sum(g[6][0] for g in groups) * w.L
-    fet_b = sum(g[6][1] for g in groups) * w.L
-    n_calls = args.steps * w.L * len(groups)
-    step_bytes = enc_b + fet_b
-    tokens = sum(g[0].tokens() for g in groups)
-    peak, peak_kind = measured_peaks()
+        res = measure_layered(w, wire, device, args.steps, args.warmup, K=args.layer_streams,
+                              distinct_layers=args.workload == "llama3_70b")
+    ps = res["pass"]
     print(json.dumps({
-        "metric": METRIC, "value": step_bytes * args.steps / total_s / 1e9, "unit": "GB/s",
+        "metric": METRIC, "value": ps["gbs"], "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": ps["ms_per_pass"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.L} layers, per-layer encode + fetch on "
-                               f"{K} encode / {K} fetch stream(s), wire {wire}, blocks "
-                               + "/".join(f"{g[0].nb}xB{g[0].B}" for g in groups),
-                   "tokens": tokens, "calls_per_step": 2 * w.L * len(groups),
-                   "layer_streams": K, "wire_ring": R},
-        "tokens_per_s": tokens * args.steps / total_s,
-        "kernels": {"encode": {"avg_us_per_call": statistics.mean(enc_t) * 1e6},
-                    "fetch": {"avg_us_per_call": statistics.mean(fet_t) * 1e6},
-                    "note": "a layer's fetch overlaps the next layer's encode (and, with more "
-                            "stream pairs, neighbouring layers' calls overlap each other), so a "
-                            "call's span includes time shared with other calls; the pass's rate "
-                            "is `value`, its time per layer `per_layer_us`"},
-        "per_layer_us": total_s / args.steps / w.L * 1e6,
+        "config": {"workload": f"{w.name}: {w.L} layers, per-layer encode + fetch, wire {wire}, "
+                               f"blocks {res['blocks']}", "tokens": res["tokens"],
+                   "layer_streams": args.layer_streams, "buffers": res["buffers"]},
+        "tokens_per_s": ps["tokens_per_s"], "per_layer_us": ps["per_layer_us"],
+        "kernels": {"encode": res["encode"], "fetch": res["fetch"]},
         "cpu_baseline": (cpu_baseline_workload(w, w.blocks[0], wire, args.cpu_seconds)
                          if "cpu" in args.legs and rank == 0 else None),
-        "peak": peak, "peak_source": peak_kind, "gpu_launches": 2 * n_calls,
+        "peak": res["peak_gbs"], "gpu_launches": 4 * w.L * len(w.blocks) * args.steps,
         "clocks": clocks.summary()}))
+
+
+def workload_lines(args, device):
+    """Compact objects for the two per-layer workloads, carried by the default
+    line: the Llama-3-70B-shaped layer-streamed fetch (80 layers, FP8, against
+    the 70%-of-8-TB/s time per layer) and the ragged INT4 sweep (36 layers,
+    blocks of 16 and 64)."""
+    import workloads
+    steps = max(3, min(args.steps, 20))
+    out = {}
+    w = workloads.llama3_70b()
+    r = measure_layered(w, "fp8", device, steps, 3, K=2, distinct_layers=True)
+    f = r["fetch"]["B64"]
+    r["fetch_target"] = {"max_us_per_layer": fetch_target_us(f["bytes_per_call"]),
+                         "median_us_per_layer": f["median_us"],
+                         "met": f["median_us"] <= fetch_target_us(f["bytes_per_call"]),
+                         "rule": "70% of the nominal ~8 TB/s for one layer's fetch bytes"}
+    out["llama3_70b"] = r
+    w = workloads.ragged()
+    out["ragged_int4"] = measure_layered(w, "int4", device, steps, 3, K=2)
+    return out
 
 
 def run_blend(args):
@@ -1074,7 +1183,9 @@ def main(argv=None):
                          "time the per-layer calls of the layer-streamed and ragged workloads; blend "
                          "times the drift-ranked token selection; hashing the host-side block "
                          "digests")
-    ap.add_argument("--legs", default="device,e2e,cpu", help="comma list of: device, e2e, cpu")
+    ap.add_argument("--legs", default="device,e2e,cpu,workloads",
+                    help="comma list of: device, e2e, cpu, workloads (the per-layer Llama-3-70B "
+                         "and ragged INT4 objects of the default line)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--cpu-procs", type=int, default=0,

@@ -22,9 +22,8 @@ import torch
 import workloads
 from oracle import paged, rope
 from oracle.numerics import round_to, ulp
+from tests.bars import K_REL, SENTINEL, compare_k, compare_v  # noqa: F401
 
-SENTINEL = -12288.0            # exact in fp32, fp16 and bf16; never a real output here
-K_REL = 2e-6
 _TORCH = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -144,18 +143,6 @@ def written_mask(c):
     return m
 
 
-def compare_k(g, e, fmt):
-    """(ok, max |err|, bar at that element) for fetched K rows [..., d]."""
-    rowmax = np.max(np.abs(e), axis=-1, keepdims=True)
-    bar = K_REL * rowmax
-    if fmt != "f32":
-        bar = bar + np.maximum(ulp(g, fmt), ulp(e, fmt))
-    err = np.abs(g - e)
-    bar = np.broadcast_to(bar, err.shape)
-    i = np.unravel_index(np.argmax(err - bar), err.shape) if err.size else ()
-    return bool(np.all(err <= bar)), float(err.max(initial=0)), float(bar[i]) if err.size else 0.0
-
-
 def compare_outputs(c, wire, gout, oout):
     rep = {}
     m = written_mask(c)
@@ -164,12 +151,7 @@ def compare_outputs(c, wire, gout, oout):
         rep[f"{name}_untouched_ok"] = bool(untouched_ok)
     ok_k, kerr, kbar = compare_k(gout["k"][m], oout["k"][m], c.out_fmt)
     rep.update(k_ok=ok_k, k_max_err=kerr, k_bar=kbar)
-    gv, ev = gout["v"][m], oout["v"][m]
-    rep["v_exact"] = bool(np.array_equal(gv, ev))
-    if wire in ("fp8", "fp8_rows") and c.out_fmt != "f32":
-        rep["v_ok"] = bool(np.all(np.abs(gv - ev) <= np.maximum(ulp(gv, c.out_fmt), ulp(ev, c.out_fmt))))
-    else:
-        rep["v_ok"] = rep["v_exact"]
+    rep["v_ok"], rep["v_exact"] = compare_v(gout["v"][m], oout["v"][m], wire, c.out_fmt)
     return rep
 
 

@@ -37,3 +37,28 @@ def test_bench_prints_the_contract_line():
     src = 2 * 2 * 2048 * 16 * 8 * 128 * 2             # K and V, 2 layers, fp16
     assert e["h2d_bytes_per_step"] >= src and e["d2h_bytes_per_step"] >= src
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+
+
+def test_per_layer_workload_objects():
+    """The per-layer objects of the default line (measure_layered) on 2-layer
+    cuts of the Llama-3-70B-shaped and ragged workloads: per-call medians for
+    every block size, the layered pass, and the fetch target arithmetic."""
+    import torch
+    import bench
+    import workloads
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    w = workloads.llama3_70b()
+    w.L = 2
+    r = bench.measure_layered(w, "fp8", dev, steps=3, warmup=3, distinct_layers=True)
+    assert set(r["fetch"]) == {"B64"} and set(r["encode"]) == {"B64"}
+    f = r["fetch"]["B64"]
+    assert f["calls"] == 3 * 2 and f["median_us"] > 0 and f["gbs"] > 0
+    assert f["bytes_per_call"] == bench.layered_bytes(w, w.blocks[0], "fp8")[1]
+    assert abs(bench.fetch_target_us(402_726_912) - 71.9) < 0.05
+    assert r["pass"]["gbs"] > 0 and r["pass"]["per_layer_us"] > 0
+    w = workloads.ragged()
+    w.L = 2
+    r = bench.measure_layered(w, "int4", dev, steps=3, warmup=3)
+    assert set(r["fetch"]) == {"B16", "B64"} and r["tokens"] == sum(b.tokens() for b in w.blocks)

@@ -1,13 +1,19 @@
 """GPU parity at the workloads' full sizes, in the launch configurations the
-benchmark uses, checked against the oracle on sampled blocks (all of their
-layers, or sampled layers) and by properties that hold at any size.
+benchmark uses, checked against the oracle on EVERY block of the checked
+layers (tests/full_parity.py: the oracle runs in spawned worker processes on
+chunks of blocks), plus properties that hold at any size.
 
 * qwen3_8b: one encode call over 36 layers x 2048 blocks, one table call, one
-  fetch call - exactly the benchmark's step.
+  fetch call - exactly the benchmark's step - for both FP8 wires; all 36
+  layers, all 2048 blocks each, are compared with the oracle.
 * llama3_70b: 80 layers fetched one layer per call on a side stream into a
-  bf16 paged cache, after per-layer encodes on the main stream.
+  bf16 paged cache, after per-layer encodes on the main stream; every block
+  of the first, a middle and the last layer is compared with the oracle, and
+  every slot of every layer is checked written.
 * ragged: 36 layers, block sizes 16 and 64 in separate calls, ragged tails,
-  INT4 (g32, fp16 scales) and FP8.
+  INT4 (g32, fp16 scales) and FP8; every block (both block sizes, every
+  padding row) of the first, a middle and the last layer is compared with
+  the oracle, and placement is checked on every layer.
 """
 import numpy as np
 import pytest
@@ -15,9 +21,10 @@ import torch
 
 import workloads
 from oracle import paged, rope
-from tests import parity
+from tests import full_parity, parity
 
 pytestmark = pytest.mark.gpu
+CHUNK_TOKENS = 4096            # tokens of one layer per oracle task
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,46 +33,55 @@ def _built():
     __graft_entry__.build()
 
 
+@pytest.fixture(scope="module")
+def pool():
+    with full_parity.OraclePool() as p:
+        yield p
+
+
 def _nan_pool(shape, dtype, device):
     return torch.full(shape, float("nan"), dtype=dtype, device=device)
 
 
-def _check_blocks(w, blk, js, layers, src_k_host, src_v_host, codes, scales, dst_k, dst_v,
-                  wire, group=32, scale_dtype="f16"):
-    """Oracle on blocks js (src arrays [len(layers), len(js), B, H, d] on the
-    host) against the GPU's wire and destination slots."""
-    n = len(js)
-    nv = blk.n_valid[js]
-    if wire == "fp8":
-        ocodes, oscales = paged.encode_fp8(src_k_host, src_v_host, np.arange(n), nv)
-        vals = paged.decode_fp8(ocodes, oscales)
-    elif wire == "fp8_rows":
-        ocodes, oscales = paged.encode_fp8_rows(src_k_host, src_v_host, np.arange(n), nv, scale_dtype)
-        vals = paged.decode_fp8_rows(ocodes, oscales)
-    else:
-        ocodes, oscales = paged.encode_int4(src_k_host, src_v_host, np.arange(n), nv, group, scale_dtype)
-        vals = paged.decode_int4(ocodes, oscales, group)
-    assert np.array_equal(codes, ocodes), "wire codes differ"
-    assert np.array_equal(scales, oscales), "wire scales differ"
-    th = rope.inv_freq(w.d, w.rope_base)
-    sent = np.full((len(layers), n, blk.B, w.H, w.d), parity.SENTINEL)
-    ek, ev = paged.fetch_rotate_scatter(vals, blk.delta_m[js], th, w.pairing, np.arange(n), sent, sent,
-                                        w.out_dtype, n_valid=nv)
-    m = np.zeros((len(layers), n, blk.B), bool)
-    for i in range(n):
-        m[:, i, :nv[i]] = True
-    ok_k, kerr, kbar = parity.compare_k(dst_k[m], ek[m], w.out_dtype)
-    assert ok_k, (kerr, kbar)
-    gv, evv = dst_v[m], ev[m]
-    if wire in ("fp8", "fp8_rows") and w.out_dtype != "f32":
-        assert np.all(np.abs(gv - evv) <= np.maximum(parity.ulp(gv, w.out_dtype), parity.ulp(evv, w.out_dtype)))
-    else:
-        assert np.array_equal(gv, evv)
-    return m
+def _host(t):
+    """A tensor's values in their stored form (bf16 as uint16 bit patterns)."""
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy()
+
+
+def submit_layer(pool, w, blk, wire, label, src_k, src_v, codes, scales, dst_k, dst_v,
+                 group=32, scale_dtype="f16"):
+    """Queue every block of one layer for the oracle, in chunks.
+
+    src_k, src_v: [num_src_slots, B, H, d] the layer's cached pool;
+    codes, scales: the layer's wire [NB, 2, H, ...]; dst_k, dst_v:
+    [num_dst_slots, B, H, d] the layer's destination pool after the fetch.
+    """
+    dev = src_k.device
+    src = torch.as_tensor(blk.src_slots.astype(np.int64), device=dev)
+    dst = torch.as_tensor(blk.dst_slots.astype(np.int64), device=dev)
+    step = max(1, CHUNK_TOKENS // blk.B)
+    for a in range(0, blk.nb, step):
+        b = min(blk.nb, a + step)
+        pool.submit(dict(
+            label=(label, a, b), wire=wire, src_fmt=w.src_dtype, out_fmt=w.out_dtype,
+            src_k=_host(src_k[src[a:b]])[None], src_v=_host(src_v[src[a:b]])[None],
+            codes=_host(codes[a:b])[None], scales=_host(scales[a:b])[None],
+            dst_k=_host(dst_k[dst[a:b]])[None], dst_v=_host(dst_v[dst[a:b]])[None],
+            n_valid=blk.n_valid[a:b].copy(), delta_m=blk.delta_m[a:b].copy(), d=w.d,
+            rope_base=w.rope_base, pairing=w.pairing, group=group, scale_dtype=scale_dtype))
+
+
+def assert_all_ok(pool, want_blocks):
+    s = full_parity.summarize(pool.results())
+    assert not s["failed"], s["failed"]
+    assert s["blocks"] == want_blocks, (s["blocks"], want_blocks)
+    return s
 
 
 @pytest.mark.parametrize("codec", ["fp8", "fp8_rows"])
-def test_qwen3_8b_benchmark_step(codec):
+def test_qwen3_8b_benchmark_step(codec, pool):
     import bench
     dev = torch.device("cuda", 0)
     w = workloads.qwen3_8b()
@@ -85,18 +101,14 @@ def test_qwen3_8b_benchmark_step(codec):
     th = rope.inv_freq(w.d, w.rope_base)
     want = paged.delta_sincos_table(np.array([4096]), th)
     assert np.all(np.abs(p.table.double().cpu().numpy() - want) <= parity.ulp(want, "f32"))
-    # oracle on sampled blocks, all 36 layers
-    r = np.random.default_rng(0)
-    js = np.unique(np.concatenate([[0, blk.nb - 1], r.choice(blk.nb, 12, replace=False)]))
-    sl = torch.as_tensor(blk.src_slots[js].astype(np.int64), device=dev)
-    dl = torch.as_tensor(blk.dst_slots[js].astype(np.int64), device=dev)
-    host = lambda t: t.double().cpu().numpy()
-    _check_blocks(w, blk, js, range(w.L), host(src_k[:, sl]), host(src_v[:, sl]),
-                  p.codes[:, js].cpu().numpy(), host(p.scales[:, js]), host(dst_k[:, dl]),
-                  host(dst_v[:, dl]), codec)
+    # the oracle on every block of every layer
+    for layer in range(w.L):
+        submit_layer(pool, w, blk, codec, f"qwen3_8b/{codec}/L{layer}", src_k[layer], src_v[layer],
+                     p.codes[layer], p.scales[layer], dst_k[layer], dst_v[layer])
+    assert_all_ok(pool, w.L * blk.nb)
 
 
-def test_llama3_70b_layer_streamed():
+def test_llama3_70b_layer_streamed(pool):
     dev = torch.device("cuda", 0)
     from kv_cache_quantization_hc_gb300 import path as kvpath
     w = workloads.llama3_70b()
@@ -122,35 +134,26 @@ def test_llama3_70b_layer_streamed():
     assert not torch.isnan(dst_k).any() and not torch.isnan(dst_v).any()
     # distinct delta-m values: one table row each, shared by all 80 layers
     assert p.n_distinct == len(np.unique(blk.delta_m)) <= 1024
-    r = np.random.default_rng(1)
-    js = np.unique(np.concatenate([[0, blk.nb - 1], r.choice(blk.nb, 6, replace=False)]))
-    layers = [0, 41, 79]
-    sl = torch.as_tensor(blk.src_slots[js].astype(np.int64), device=dev)
-    dl = torch.as_tensor(blk.dst_slots[js].astype(np.int64), device=dev)
-    host = lambda t: t.double().cpu().numpy()
-    sk = np.concatenate([host(workloads.device_pool(w, blk, range(l, l + 1), 0, dev)[:, sl]) for l in layers])
-    sv = np.concatenate([host(workloads.device_pool(w, blk, range(l, l + 1), 1, dev)[:, sl]) for l in layers])
-    li = torch.as_tensor(layers, device=dev)
-    _check_blocks(w, blk, js, layers, sk, sv, p.codes[li][:, js].cpu().numpy(),
-                  host(p.scales[li][:, js]), host(dst_k[li][:, dl]), host(dst_v[li][:, dl]), "fp8")
+    layers = [0, w.L // 2, w.L - 1]
+    for layer in layers:
+        k = workloads.device_pool(w, blk, range(layer, layer + 1), 0, dev)[0]
+        v = workloads.device_pool(w, blk, range(layer, layer + 1), 1, dev)[0]
+        submit_layer(pool, w, blk, "fp8", f"llama3_70b/L{layer}", k, v, p.codes[layer],
+                     p.scales[layer], dst_k[layer], dst_v[layer])
+    assert_all_ok(pool, len(layers) * blk.nb)
 
 
 @pytest.mark.parametrize("wire", ["int4", "fp8"])
-def test_ragged_sweep(wire):
+def test_ragged_sweep(wire, pool):
     dev = torch.device("cuda", 0)
     from kv_cache_quantization_hc_gb300 import path as kvpath
     w = workloads.ragged()
-    check_layers = [0, 17, 35]
+    check_layers = [0, w.L // 2, w.L - 1]
     all_layers = range(w.L) if wire == "int4" else check_layers
+    want = 0
     for bi, blk in enumerate(w.blocks):
         p = kvpath.from_blocks(w, blk, wire, device=dev, n_layers=1, scale_dtype="f16")
         p.build_table()
-        r = np.random.default_rng(10 + bi)
-        tails = np.flatnonzero(blk.n_valid < blk.B)
-        js = np.unique(np.concatenate([[0, blk.nb - 1], tails[:6], r.choice(blk.nb, 6, replace=False)]))
-        sl = torch.as_tensor(blk.src_slots[js].astype(np.int64), device=dev)
-        dl = torch.as_tensor(blk.dst_slots[js].astype(np.int64), device=dev)
-        host = lambda t: t.double().cpu().numpy()
         shape = (1, blk.num_dst_slots, blk.B, w.H, w.d)
         for layer in all_layers:
             k = workloads.device_pool(w, blk, range(layer, layer + 1), 0, dev)
@@ -169,6 +172,7 @@ def test_ragged_sweep(wire):
             untouched = (dk[0] == parity.SENTINEL).all(-1).all(-1)
             assert torch.equal(untouched, ~written)
             if layer in check_layers:
-                _check_blocks(w, blk, js, [layer], host(k[:, sl]), host(v[:, sl]),
-                              p.codes[:, js].cpu().numpy(), host(p.scales[:, js]),
-                              host(dk[:, dl]), host(dv[:, dl]), wire)
+                submit_layer(pool, w, blk, wire, f"ragged/{wire}/B{blk.B}/L{layer}", k[0], v[0],
+                             p.codes[0], p.scales[0], dk[0], dv[0])
+                want += blk.nb
+    assert_all_ok(pool, want)
