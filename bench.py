@@ -35,7 +35,8 @@ METRIC = "KV fetch+rotate+scatter GB/s and tokens/s; % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = {
-    "k_encode": ["encode.cu", "encode_common.cuh", "crc_math.h", "hc_internal.cuh", "fastdiv.h"],
+    "k_encode": ["encode.cu", "encode_common.cuh", "crc_math.h", "crc_fields.cuh", "hc_internal.cuh",
+                 "fastdiv.h"],
     "k_fetch": ["fetch_impl.cuh", "fetch_fp8.cu", "hc_internal.cuh", "fastdiv.h"],
     "k_encode_fp8_rows": ["encode_rows.cu", "encode_common.cuh", "hc_internal.cuh", "fastdiv.h"],
     "k_fetch_fp8_rows": ["fetch_impl.cuh", "fetch_fp8_rows.cu", "hc_internal.cuh", "fastdiv.h"],
@@ -374,7 +375,8 @@ def run_crc(args, p, device, src_k, src_v):
     peak, _ = measured_peaks()
     out_d = {"kernel": "k_crc32", "units": p.L * p.nb, "bytes_per_launch": nbytes, "launches": reps,
              "avg_ms": avg * 1e3, "gbs": nbytes / avg / 1e9, "frac": nbytes / avg / 1e9 / peak,
-             "bound": "shared-memory table lookups (the traffic is read-only HBM)"}
+             "bound": "integer ALU: field extraction for the 5-bit table lookups (the traffic is "
+                      "read-only HBM)"}
     if args.codec == "fp8":
         slab_crc = torch.empty((p.L, p.nb, 2, p.H), dtype=torch.int32, device=device)
 
@@ -1003,7 +1005,8 @@ def measure_layered(w, wire, device, steps, warmup, K=2, distinct_layers=False):
             per_kernel[name][f"B{g['blk'].B}"] = {
                 "median_us": med * 1e6, "min_us": min(ts) * 1e6, "calls": len(ts),
                 "bytes_per_call": b, "gbs": b / med / 1e9, "frac": b / med / 1e9 / peak,
-                "tokens_per_s": g["blk"].tokens() / med}
+                # context tokens through all layers per second at this call's rate
+                "tokens_per_s": g["blk"].tokens() / (med * w.L)}
     pass_bytes = sum(g["bytes"][0] + g["bytes"][1] for g in groups) * w.L
     tokens = sum(g["blk"].tokens() for g in groups)
     out = {"layers": w.L, "tokens": tokens, "wire": wire,

@@ -129,8 +129,11 @@ int hc_encode_fp8(const void* paged_k, const void* paged_v, const hc_paged_desc*
  * hc_crc32 defines it) of the slab's block_size*d_head code bytes followed by
  * the 4 bytes of its fp32 scale - hc_crc32(codes, B*d, B*d, scales, 4, 4,
  * n_slabs).  For fp16/bf16 sources the CRC is folded into the encode as the
- * codes are produced; for fp32 sources the call runs the CRC kernel after the
- * encode.  Slabs of skipped blocks get no CRC.
+ * codes are produced, and the slabs of a skipped block (a bad src_slots[j] or
+ * n_valid[j]) get no CRC: their crc entries are left as they were.  For fp32
+ * sources the call runs the CRC kernel over every slab after the encode, so a
+ * skipped block's entries hold the CRC of its wire bytes as they stand (the
+ * bytes it had before the call).
  * [HyperCache page, "Example output" part B: blocks stored with CRC32.]
  *
  *   crc : device u32 [n_layers][n_blocks][2][n_kv_heads], 4-byte aligned

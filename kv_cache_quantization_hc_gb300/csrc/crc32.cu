@@ -5,100 +5,190 @@
 //
 // The variant is CRC-32/ISO-HDLC (zlib, PNG): polynomial 0x04C11DB7 processed
 // bit-reflected, register initialised to 0xFFFFFFFF, final xor 0xFFFFFFFF.
+// The GF(2) arithmetic is in crc_math.h, the table-driven linear maps in
+// crc_fields.cuh.
 //
-// Polynomials mod P are held bit-reflected: bit 31 - i is the coefficient of
-// x^i, so multiplying by x is a right shift that folds the x^31 coefficient
-// back with the reflected polynomial 0xEDB88320.  After n message bytes the
-// register is  init * x^(8n) + (a term linear in the message)  mod P, so a
-// message can be cut into pieces whose registers (started at 0) are computed
-// independently, moved to the end of the message by multiplying with
-// x^(8 * bytes after the piece), and xor-ed.
+// A register that starts at 0 does not change over leading zero bytes, and
+// after n message bytes it is  (a term linear in the message)  while the
+// initial register contributes init * x^(8n) mod P.  So a message can be cut
+// into pieces whose registers are computed independently and moved to the
+// message's end by multiplying with x^(8 * bytes after the piece).
 //
-// One warp per unit: lane k < 31 runs its piece of the a part, lane 31 the
-// rest of a and all of b.  A lane consumes its piece 128 bytes at a time (eight
-// 16-byte loads in flight), each 16-byte word in one step of the
-// slicing-by-16 table method (Kounavis and Berry, "Novel table lookup-based
-// algorithms for high-performance CRC generation", IEEE Trans. Computers
-// 57(11), 2008): table k maps a byte to its register contribution when k
-// zero bytes follow it.  The 16 tables (16 KiB) are built in shared memory by
-// each CTA.
+// One warp per unit, persistent CTAs.  A unit is two segments: the 16-byte
+// words of a (16-byte aligned), then the ragged rest of a followed by b, read
+// byte by byte and padded in front with zero bytes to whole 16-byte words
+// (leading zeros leave a zero-started register unchanged).  A segment is cut
+// into rows of 32 words, 512 bytes, and padded in front with zero words to a
+// whole number of groups of kGroup rows.  Lane l takes word l of every row, so
+// a warp's loads are 512 contiguous bytes.  Per group of rows a lane moves its
+// register past the group (x^(8 * 512 * kGroup)) and adds each of its words'
+// contributions, read from the map of that word's row position; the register
+// then describes everything the lane has read, with every other lane's bytes
+// taken as zero, positioned at the end of the lane's last word.  A butterfly
+// over the lanes (the lower lane of each pair moves its register 16 * 2^j
+// bytes on and adds its partner's) leaves lane 0 with the segment's register
+// at the segment's end.  Lane 0 moves the first segment's register past the
+// second segment and adds the second's, the initial register's term and the
+// final xor.
+//
+// Why rows: the previous design gave each lane a contiguous piece of the unit,
+// so a warp's 16-byte loads touched 32 lines 1 KiB apart; that layout, plus
+// byte-indexed tables whose lookups collide, held the kernel to 2.0 TB/s.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "crc_fields.cuh"
 #include "crc_math.h"
 #include "hc_internal.cuh"
 
 namespace hc {
 namespace {
 
-constexpr uint32_t kPolyReflected = kCrcPolyReflected;
-constexpr int kTables = 16;
-inline uint32_t x_pow_bytes(uint64_t n) { return crc_x_pow_bytes(n); }
+// Tables of one CTA, filled from the host-computed images in CrcParams.
+struct CrcShared {
+  FieldMap<128> word[kCrcGroup];  // word at row position g of a group -> register at the group's end
+  FieldMap<32> group;             // a register -> the register kGroup rows later
+  FieldMap<32> level[5];          // a register -> the register 16 * 2^j bytes later
+};
 
-// One 16-byte word (bytes in memory order) into register r.
-__device__ __forceinline__ uint32_t step16(const uint32_t (*T)[256], uint32_t r, uint4 w) {
-  const uint32_t v = w.x ^ r;
-  uint32_t c = T[15][v & 0xff] ^ T[14][(v >> 8) & 0xff] ^ T[13][(v >> 16) & 0xff] ^ T[12][v >> 24];
-  c ^= T[11][w.y & 0xff] ^ T[10][(w.y >> 8) & 0xff] ^ T[9][(w.y >> 16) & 0xff] ^ T[8][w.y >> 24];
-  c ^= T[7][w.z & 0xff] ^ T[6][(w.z >> 8) & 0xff] ^ T[5][(w.z >> 16) & 0xff] ^ T[4][w.z >> 24];
-  c ^= T[3][w.w & 0xff] ^ T[2][(w.w >> 8) & 0xff] ^ T[1][(w.w >> 16) & 0xff] ^ T[0][w.w >> 24];
-  return c;
+__device__ void build_maps(const CrcParams& p, CrcShared& s) {
+  for (int g = 0; g < kCrcGroup; ++g) fill_field_map<128>(s.word[g], p.img_word[g]);
+  fill_field_map<32>(s.group, p.img_group);
+  for (int j = 0; j < 5; ++j) fill_field_map<32>(s.level[j], p.img_level[j]);
+  __syncthreads();
 }
 
-__device__ __forceinline__ uint32_t step1(const uint32_t (*T)[256], uint32_t r, uint32_t byte) {
-  return (r >> 8) ^ T[0][(r ^ byte) & 0xff];
-}
-
-__global__ void __launch_bounds__(kThreads) k_crc32(CrcParams p) {
-  __shared__ uint32_t T[kTables][256];
-  {
-    const uint32_t t = threadIdx.x;  // kThreads == 256: one table entry per thread
-    uint32_t c = t;
-    for (int i = 0; i < 8; ++i) c = (c >> 1) ^ ((c & 1u) ? kPolyReflected : 0u);
-    T[0][t] = c;
-    __syncthreads();
-    for (int k = 1; k < kTables; ++k) {
-      c = (c >> 8) ^ T[0][c & 0xff];
-      T[k][t] = c;
-    }
-    __syncthreads();
+__device__ __forceinline__ uint32_t lane_tree(const CrcShared& s, uint32_t r, int lane) {
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, r, 1 << j);
+    const uint32_t moved = apply_map(s.level[j], r);
+    r = ((lane >> j) & 1) ? r : (moved ^ other);
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t u = blockIdx.x * kWarps + warp;
-  if (u >= p.n_units) return;
-  const uint8_t* a = p.a + static_cast<int64_t>(u) * p.a_stride;
-  const int64_t begin = lane * p.chunk;
-  const int64_t end = lane < 31 ? begin + p.chunk : p.a_bytes;
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word_contrib(const FieldMap<128>& m, uint4 w) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+  return apply_map<128>(m, v);
+}
+
+// Segment 1: the n_words 16-byte words at `a`.  Only the first group can
+// hold front padding; the rest read at a pointer that steps a group at a time.
+__device__ __forceinline__ uint32_t aligned_segment(const CrcShared& s, const uint4* a,
+                                                    int64_t n_words, int lane) {
+  constexpr int kGroupWords = 32 * kCrcGroup;
+  const int groups = static_cast<int>((n_words + kGroupWords - 1) / kGroupWords);
+  const int64_t first = n_words - static_cast<int64_t>(groups) * kGroupWords + lane;  // > lane - 128
   uint32_t r = 0;
-  int64_t pos = begin;
-  for (; pos + 128 <= end; pos += 128) {
-    uint4 w[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = __ldcs(reinterpret_cast<const uint4*>(a + pos) + i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r = step16(T, r, w[i]);
+  for (int g = 0; g < kCrcGroup; ++g) {
+    const int64_t k = first + g * 32;
+    r ^= word_contrib(s.word[g], k >= 0 ? __ldcs(a + k) : make_uint4(0u, 0u, 0u, 0u));
   }
-  for (; pos + 16 <= end; pos += 16) r = step16(T, r, __ldcs(reinterpret_cast<const uint4*>(a + pos)));
-  for (; pos < end; ++pos) r = step1(T, r, a[pos]);
-  if (lane == 31 && p.b_bytes > 0) {
-    const uint8_t* b = p.b + static_cast<int64_t>(u) * p.b_stride;
-    for (int64_t i = 0; i < p.b_bytes; ++i) r = step1(T, r, b[i]);
-  }
-  r = gf2_mul(r, p.lane_shift[lane]);
+  const uint4* ptr = a + (first + kGroupWords);
+#pragma unroll 2
+  for (int gi = 1; gi < groups; ++gi, ptr += kGroupWords) {
+    uint4 w[kCrcGroup];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) r ^= __shfl_xor_sync(0xffffffffu, r, o);
-  if (lane == 0) p.crc[u] = r ^ p.init_term;
+    for (int g = 0; g < kCrcGroup; ++g) w[g] = __ldcs(ptr + g * 32);
+    uint32_t c = apply_map(s.group, r);
+#pragma unroll
+    for (int g = 0; g < kCrcGroup; ++g) c ^= word_contrib(s.word[g], w[g]);
+    r = c;
+  }
+  return lane_tree(s, r, lane);
+}
+
+// Segment 2: t bytes at `at`, then nb bytes at `b`, read byte by byte.
+__device__ __forceinline__ uint32_t byte_segment(const CrcShared& s, const uint8_t* at, int64_t t,
+                                                 const uint8_t* b, int64_t nb, int lane) {
+  const int64_t len = t + nb;
+  const int64_t n_words = (len + 15) / 16;
+  const int64_t front = 16 * n_words - len;  // zero bytes in front
+  const int64_t groups = (n_words + 32 * kCrcGroup - 1) / (32 * kCrcGroup);
+  const int64_t first = n_words - groups * 32 * kCrcGroup + lane;
+  uint32_t r = 0;
+  for (int64_t gi = 0; gi < groups; ++gi) {
+    uint32_t c = apply_map(s.group, r);
+#pragma unroll
+    for (int g = 0; g < kCrcGroup; ++g) {
+      const int64_t k = first + (gi * kCrcGroup + g) * 32;
+      uint32_t v[4] = {0u, 0u, 0u, 0u};
+      if (k >= 0) {
+        for (int i = 0; i < 16; ++i) {
+          const int64_t m = 16 * k + i - front;  // byte of the segment
+          const uint32_t byte = m < 0 ? 0u : (m < t ? at[m] : b[m - t]);
+          v[i >> 2] |= byte << (8 * (i & 3));
+        }
+      }
+      c ^= apply_map<128>(s.word[g], v);
+    }
+    r = c;
+  }
+  return lane_tree(s, r, lane);
+}
+
+__global__ void __launch_bounds__(kThreads) k_crc32(const __grid_constant__ CrcParams p) {
+  __shared__ CrcShared maps;
+  build_maps(p, maps);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t words = p.a_bytes >> 4, t = p.a_bytes & 15;
+  for (uint32_t u = blockIdx.x * kWarps + warp; u < p.n_units; u += gridDim.x * kWarps) {
+    const uint8_t* a = p.a + static_cast<int64_t>(u) * p.a_stride;
+    uint32_t r1 = words ? aligned_segment(maps, reinterpret_cast<const uint4*>(a), words, lane) : 0u;
+    uint32_t r2 = 0;
+    if (t + p.b_bytes > 0) {
+      const uint8_t* b = p.b_bytes > 0 ? p.b + static_cast<int64_t>(u) * p.b_stride : nullptr;
+      r2 = byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane);
+    }
+    if (lane == 0) p.crc[u] = gf2_mul(r1, p.seg2_shift) ^ r2 ^ p.init_term;
+  }
+}
+
+// The images of the maps' single-bit inputs; they depend on nothing but the
+// polynomial and kCrcGroup, so they are computed once per process.
+struct CrcImages {
+  uint32_t word[kCrcGroup][128], group[32], level[5][32];
+};
+
+const CrcImages& crc_images() {
+  static CrcImages img;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    // Message bit q of a 16-byte word (bit q % 8 of byte q / 8; the reflected
+    // order processes bit 0 of byte 0 first) is the coefficient of
+    // x^(127 - q), and x^32 more moves it into the register after the word.
+    for (int g = 0; g < kCrcGroup; ++g) {
+      const uint32_t later = crc_x_pow_bytes(512u * (kCrcGroup - 1 - g));
+      for (int q = 0; q < 128; ++q) img.word[g][q] = gf2_mul(crc_x_pow_bits(159 - q), later);
+    }
+    // A register bit j (bit 31 - i holds x^i) times the shift.
+    const uint32_t grp = crc_x_pow_bytes(512u * kCrcGroup);
+    for (int j = 0; j < 32; ++j) img.group[j] = gf2_mul(1u << j, grp);
+    for (int l = 0; l < 5; ++l) {
+      const uint32_t sh = crc_x_pow_bytes(16u << l);
+      for (int j = 0; j < 32; ++j) img.level[l][j] = gf2_mul(1u << j, sh);
+    }
+  });
+  return img;
 }
 
 }  // namespace
 
 cudaError_t launch_crc32(const CrcParams& in, cudaStream_t s) {
   CrcParams p = in;
-  p.chunk = (p.a_bytes / (32 * 128)) * 128;
+  const CrcImages& img = crc_images();
+  std::memcpy(p.img_word, img.word, sizeof img.word);
+  std::memcpy(p.img_group, img.group, sizeof img.group);
+  std::memcpy(p.img_level, img.level, sizeof img.level);
   const uint64_t n = static_cast<uint64_t>(p.a_bytes + p.b_bytes);
-  for (int k = 0; k < 32; ++k) {
-    const uint64_t after = k < 31 ? n - static_cast<uint64_t>((k + 1) * p.chunk) : 0;
-    p.lane_shift[k] = x_pow_bytes(after);
-  }
-  p.init_term = gf2_mul(0xFFFFFFFFu, x_pow_bytes(n)) ^ 0xFFFFFFFFu;
-  const uint32_t grid = (p.n_units + kWarps - 1) / kWarps;
+  p.seg2_shift = crc_x_pow_bytes(static_cast<uint64_t>((p.a_bytes & 15) + p.b_bytes));
+  p.init_term = gf2_mul(0xFFFFFFFFu, crc_x_pow_bytes(n)) ^ 0xFFFFFFFFu;
+  const int64_t ctas = (static_cast<int64_t>(p.n_units) + kWarps - 1) / kWarps;
+  const uint32_t grid = static_cast<uint32_t>(
+      std::min<int64_t>(ctas, static_cast<int64_t>(device_sm_count()) * kCrcCtasPerSm));
   k_crc32<<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

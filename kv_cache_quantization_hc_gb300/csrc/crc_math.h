@@ -27,15 +27,18 @@ __host__ __device__ inline uint32_t gf2_mul(uint32_t a, uint32_t b) {
   return p;
 }
 
-// x^(8n) mod P.
-inline uint32_t crc_x_pow_bytes(uint64_t n) {
+// x^e mod P.
+inline uint32_t crc_x_pow_bits(uint64_t e) {
   uint32_t result = 0x80000000u;  // 1
   uint32_t base = 0x40000000u;    // x
-  for (uint64_t e = 8 * n; e; e >>= 1) {
+  for (; e; e >>= 1) {
     if (e & 1) result = gf2_mul(result, base);
     base = gf2_mul(base, base);
   }
   return result;
 }
+
+// x^(8n) mod P.
+inline uint32_t crc_x_pow_bytes(uint64_t n) { return crc_x_pow_bits(8 * n); }
 
 }  // namespace hc

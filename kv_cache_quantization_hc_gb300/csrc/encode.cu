@@ -55,6 +55,7 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "crc_fields.cuh"
 #include "crc_math.h"
 #include "encode_common.cuh"
 
@@ -272,109 +273,61 @@ __device__ __forceinline__ void load_rows(const EncodeParams& p, const Where& w,
 // ---------------------------------------------------------------- Fused CRC
 // The FP8 encoder can also write the CRC-32/ISO-HDLC of every slab - its
 // B x d code bytes, then its 4-byte fp32 scale - the unit hc_crc32 computes
-// for a = codes (B d bytes apart), b = scales (4 bytes apart).  CRCs are
-// linear over GF(2) (see crc_math.h), so each lane folds its own code words
-// as it produces them: a lane's pieces (8 bytes per pass) lie 256 bytes
-// apart, so its register moves to the next piece's end by a multiplication
-// with K = x^(8*256), done with four byte tables built from crc_kbasis, and
-// takes in the piece's own CRC by slicing-by-8 (persistent CTAs instead build
-// position tables once, which do both in 8 lookups).  After the last pass a
-// butterfly over the lanes (crc_lane_tree) brings the warp's register to the
-// end of the sub-slab, the sub-slabs of a slab combine in shared memory
-// (crc_sub), and the scale bytes, the initial register and the final xor are
-// added.
-struct CrcTables {
-  uint32_t t[8][256];       // t[k][v]: register contribution of byte v followed by k zero bytes
-  uint32_t m[4][256];       // m[b][v]: (v << 8b) * K mod P
-  uint32_t lvl[5][4][256];  // lvl[j][b][v]: (v << 8b) * x^(64 * 2^j) mod P (the lane tree)
-  uint32_t basis[5][32];    // x^(64 * 2^j) times each single-bit value
+// for a = codes (B d bytes apart), b = scales (4 bytes apart).  Everything a
+// CRC does is linear over GF(2) (crc_math.h), and each linear map is applied
+// by lookups on 5-bit fields of its input (crc_fields.cuh), whose tables a
+// warp reads without bank collisions.  A lane's code pieces (8 bytes per
+// pass) lie 256 bytes apart; the map of pass i takes a piece straight to its
+// contribution at the end of the lane's last piece, so a pass costs 13
+// lookups.  After the last pass a butterfly over the lanes (crc_lane_tree)
+// brings the warp's register to the end of the sub-slab, the sub-slabs of a
+// slab combine in shared memory (crc_sub), and the register is moved past the
+// scale's 4 bytes, which are added with the initial register's term and the
+// final xor.  The images of the maps' single-bit inputs come from the host
+// (make_slab_crc_constants); each CTA fills its tables once.
+template <int kPasses>
+struct SlabCrcMaps {
+  FieldMap<64> pos[kPasses];  // pass i's 8 code bytes -> the lane's register at its last piece
+  FieldMap<32> level[5];      // a register -> the register 8 * 2^j bytes later
+  FieldMap<32> tail;          // a register -> the register after the 4 scale bytes
+  FieldMap<32> scale;         // the scale's 4 bytes -> the register after them
 };
 
-__device__ __forceinline__ void build_crc_tables(const EncodeParams& p, CrcTables& tab) {
-  for (int v = threadIdx.x; v < 256; v += kThreads) {
-    uint32_t c = v;
-    for (int i = 0; i < 8; ++i) c = crc_times_x(c);
-    tab.t[0][v] = c;
-  }
-  for (int e = threadIdx.x; e < 5 * 32; e += kThreads)
-    tab.basis[e / 32][e % 32] = gf2_mul(1u << (e % 32), p.crc_level[e / 32]);
-  __syncthreads();
-  for (int e = threadIdx.x; e < 5 * 4 * 256; e += kThreads) {
-    const int j = e / 1024, b = (e / 256) % 4, v = e % 256;
-    uint32_t m = 0;
-    for (int q = 0; q < 8; ++q)
-      if ((v >> q) & 1) m ^= tab.basis[j][8 * b + q];
-    tab.lvl[j][b][v] = m;
-  }
-  for (int v = threadIdx.x; v < 256; v += kThreads) {
-    uint32_t c = tab.t[0][v];
-    for (int k = 1; k < 8; ++k) {
-      c = (c >> 8) ^ tab.t[0][c & 0xff];
-      tab.t[k][v] = c;
-    }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      uint32_t m = 0;
-      for (int j = 0; j < 8; ++j)
-        if ((v >> j) & 1) m ^= p.crc_kbasis[8 * b + j];
-      tab.m[b][v] = m;
-    }
-  }
-  __syncthreads();
-}
-
-// Position tables (persistent launch): pos[i][k][v] is the contribution of
-// byte v at byte k of a lane's pass-i piece, moved to the end of the lane's
-// last piece - the byte table t[7-k] multiplied by K once per later pass.
-// With them a pass costs 8 lookups instead of 12 (no K step).
 template <int kPasses>
-__device__ __forceinline__ void build_crc_pos_tables(const CrcTables& tab, uint32_t* pos) {
-  for (int e = threadIdx.x; e < kPasses * 8 * 256; e += kThreads) {
-    const int i = e / 2048, k = (e / 256) % 8, v = e % 256;
-    uint32_t c = tab.t[7 - k][v];
-    for (int n = i; n < kPasses - 1; ++n)
-      c = tab.m[0][c & 0xff] ^ tab.m[1][(c >> 8) & 0xff] ^ tab.m[2][(c >> 16) & 0xff] ^ tab.m[3][c >> 24];
-    pos[e] = c;
-  }
+__device__ __forceinline__ void build_slab_crc_maps(const EncodeParams& p, SlabCrcMaps<kPasses>& m) {
+  for (int i = 0; i < kPasses; ++i) fill_field_map<64>(m.pos[i], p.crc_img_pos[i]);
+  for (int j = 0; j < 5; ++j) fill_field_map<32>(m.level[j], p.crc_img_level[j]);
+  fill_field_map<32>(m.tail, p.crc_img_tail);
+  fill_field_map<32>(m.scale, p.crc_img_scale);
   __syncthreads();
 }
 
-__device__ __forceinline__ uint32_t crc_pos(const uint32_t* pos_i, uint2 c) {
-  const uint32_t(*t)[256] = reinterpret_cast<const uint32_t(*)[256]>(pos_i);
-  return t[0][c.x & 0xff] ^ t[1][(c.x >> 8) & 0xff] ^ t[2][(c.x >> 16) & 0xff] ^ t[3][c.x >> 24] ^
-         t[4][c.y & 0xff] ^ t[5][(c.y >> 8) & 0xff] ^ t[6][(c.y >> 16) & 0xff] ^ t[7][c.y >> 24];
+__device__ __forceinline__ uint32_t crc_piece(const FieldMap<64>& m, uint2 c) {
+  const uint32_t v[2] = {c.x, c.y};
+  return apply_map<64>(m, v);
 }
 
 // The warp's register from each lane's (positioned at the end of the lane's
 // last piece; lane l's pieces start at byte 8l of each 256-byte pass block):
 // a butterfly in which the lower lane of each pair moves its value 8 * 2^j
-// bytes on (a table multiplication by x^(64 * 2^j)) and adds its partner's.
-// Lane 0 ends with the value at the end of the sub-slab.
-__device__ __forceinline__ uint32_t crc_lane_tree(const CrcTables& tab, uint32_t acc, int lane) {
+// bytes on and adds its partner's.  Lane 0 ends with the value at the end of
+// the sub-slab.
+__device__ __forceinline__ uint32_t crc_lane_tree(const FieldMap<32> (&level)[5], uint32_t acc,
+                                                  int lane) {
 #pragma unroll
   for (int j = 0; j < 5; ++j) {
     const uint32_t other = __shfl_xor_sync(0xffffffffu, acc, 1 << j);
-    const uint32_t moved = tab.lvl[j][0][acc & 0xff] ^ tab.lvl[j][1][(acc >> 8) & 0xff] ^
-                           tab.lvl[j][2][(acc >> 16) & 0xff] ^ tab.lvl[j][3][acc >> 24];
+    const uint32_t moved = apply_map(level[j], acc);
     acc = ((lane >> j) & 1) ? acc : (moved ^ other);
   }
   return acc;
-}
-
-// acc * K + CRC(8 code bytes c), register started at 0.
-__device__ __forceinline__ uint32_t crc_fold(const CrcTables& tab, uint32_t acc, uint2 c) {
-  const uint32_t mk = tab.m[0][acc & 0xff] ^ tab.m[1][(acc >> 8) & 0xff] ^
-                      tab.m[2][(acc >> 16) & 0xff] ^ tab.m[3][acc >> 24];
-  return mk ^ tab.t[7][c.x & 0xff] ^ tab.t[6][(c.x >> 8) & 0xff] ^ tab.t[5][(c.x >> 16) & 0xff] ^
-         tab.t[4][c.x >> 24] ^ tab.t[3][c.y & 0xff] ^ tab.t[2][(c.y >> 8) & 0xff] ^
-         tab.t[1][(c.y >> 16) & 0xff] ^ tab.t[0][c.y >> 24];
 }
 
 template <typename SrcT, int D, bool kCrc>
 __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where& w,
                                              const SlotInfo& si, int chunk, int rr, int warp,
                                              int lane, float* s_amax, uint32_t* s_crc,
-                                             const CrcTables* tab, const uint32_t* pos,
+                                             const SlabCrcMaps<EncodeGeom<D>::kPasses>* maps,
                                              const Raw8<SrcT> (&raw)[EncodeGeom<D>::kPasses]) {
   using G = EncodeGeom<D>;
   const int bad = w.active ? slot_errors(p, si) : 0;
@@ -417,19 +370,19 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
       for (int i = 0; i < G::kPasses; ++i) {
         const uint2 c = fp8x8_corrected(raw[i], s, r);
         __stcs(dst + i * kPassStride, c);
-        if constexpr (kCrc) acc = pos ? acc ^ crc_pos(pos + i * 2048, c) : crc_fold(*tab, acc, c);
+        if constexpr (kCrc) acc ^= crc_piece(maps->pos[i], c);
       }
     } else {
 #pragma unroll
       for (int i = 0; i < G::kPasses; ++i) {
         const uint2 c = fp8x8_divide(raw[i], s);
         __stcs(dst + i * kPassStride, c);
-        if constexpr (kCrc) acc = pos ? acc ^ crc_pos(pos + i * 2048, c) : crc_fold(*tab, acc, c);
+        if constexpr (kCrc) acc ^= crc_piece(maps->pos[i], c);
       }
     }
     if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
     if constexpr (kCrc) {
-      acc = crc_lane_tree(*tab, acc, lane);  // lane 0: the sub-slab's register
+      acc = crc_lane_tree(maps->level, acc, lane);  // lane 0: the sub-slab's register
       if (wps > 1) {
         if (lane == 0) s_crc[warp] = acc;
         __syncthreads();
@@ -441,9 +394,7 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
       }
       if (w.sub == 0 && lane == 0) {
         const uint32_t sb = __float_as_uint(s);  // the scale's 4 bytes, little-endian
-        const uint32_t scale_crc = tab->t[3][sb & 0xff] ^ tab->t[2][(sb >> 8) & 0xff] ^
-                                   tab->t[1][(sb >> 16) & 0xff] ^ tab->t[0][sb >> 24];
-        p.crc[w.slab] = gf2_mul(acc, p.crc_tail) ^ scale_crc ^ p.crc_init;
+        p.crc[w.slab] = apply_map(maps->tail, acc) ^ apply_map(maps->scale, sb) ^ p.crc_init;
       }
     }
     return;
@@ -684,24 +635,18 @@ __global__ void __launch_bounds__(kThreads, HC_ENCODE_WIDE_MIN_BLOCKS) k_encode_
 // kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
 // kCrc: the FP8 wire with the fused slab CRC (16-bit sources).
 template <typename SrcT, int D, int kWire, bool kFlat, int kGroupLog2, bool kCrc = false>
-__global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams p) {
+__global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(const __grid_constant__ EncodeParams p) {
   using G = EncodeGeom<D>;
   constexpr bool kDoubleBuffer = !kFlat && sizeof(SrcT) == 2;
   static_assert(!kCrc || (kWire == 0 && sizeof(SrcT) == 2), "fused CRC: FP8, 16-bit sources");
   __shared__ float s_amax[2][kWarps];
   __shared__ uint32_t s_crc[2][kWarps];
-  using Tab = typename std::conditional<kCrc, CrcTables, char>::type;
-  __shared__ Tab crc_tab;
-  const CrcTables* tab = nullptr;
-  const uint32_t* pos = nullptr;
+  using Maps = SlabCrcMaps<G::kPasses>;
+  __shared__ typename std::conditional<kCrc, Maps, char>::type crc_maps;
+  const Maps* maps = nullptr;
   if constexpr (kCrc) {
-    build_crc_tables(p, crc_tab);
-    tab = &crc_tab;
-    if constexpr (!kFlat) {  // persistent CTAs build the position tables once
-      extern __shared__ uint32_t crc_pos_smem[];
-      build_crc_pos_tables<G::kPasses>(crc_tab, crc_pos_smem);
-      pos = crc_pos_smem;
-    }
+    build_slab_crc_maps(p, crc_maps);
+    maps = &crc_maps;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = lane % G::kChunksPerRow, rr = lane / G::kChunksPerRow;
@@ -712,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(EncodeParams
   auto process = [&](const Where& w, const SlotInfo& si, const Raw8<SrcT>(&raw)[G::kPasses],
                      int parity) {
     if constexpr (kWire == 0)
-      quantize_fp8<SrcT, D, kCrc>(p, w, si, chunk, rr, warp, lane, s_amax[parity], s_crc[parity], tab,
-                                  pos, raw);
+      quantize_fp8<SrcT, D, kCrc>(p, w, si, chunk, rr, warp, lane, s_amax[parity], s_crc[parity],
+                                  maps, raw);
     else
       quantize_int4<SrcT, D, kWire == 1, kGroupLog2>(p, w, si, chunk, rr, lane, raw);
   };
@@ -814,15 +759,26 @@ cudaError_t launch_encode_fp8(int dtype, int d, const EncodeParams& p, cudaStrea
 }
 
 void make_slab_crc_constants(int d, int block_size, EncodeParams* p) {
-  const uint32_t k = crc_x_pow_bytes(256);
-  for (int j = 0; j < 32; ++j) p->crc_kbasis[j] = gf2_mul(1u << j, k);
-  for (int j = 0; j < 5; ++j) p->crc_level[j] = crc_x_pow_bytes(8u << j);
+  const int passes = kRowsPerWarp * d / 256;  // 8-byte pieces per lane per sub-slab
+  // A register bit j (bit 31 - i holds x^i) times x^e.
+  auto reg_images = [](uint32_t* img, uint64_t bits) {
+    const uint32_t m = crc_x_pow_bits(bits);
+    for (int j = 0; j < 32; ++j) img[j] = gf2_mul(1u << j, m);
+  };
+  // Bit q of pass i's piece (bit q % 8 of byte q / 8, processed first for
+  // q = 0) is the coefficient of x^(63 - q); x^32 moves it into the register
+  // after the piece, and x^(8 * 256) per later pass to the lane's last piece.
+  for (int i = 0; i < passes; ++i)
+    for (int q = 0; q < 64; ++q)
+      p->crc_img_pos[i][q] = crc_x_pow_bits(95 - q + 2048ull * (passes - 1 - i));
+  for (int j = 0; j < 5; ++j) reg_images(p->crc_img_level[j], 64ull << j);
+  reg_images(p->crc_img_tail, 32);
+  for (int q = 0; q < 32; ++q) p->crc_img_scale[q] = crc_x_pow_bits(63 - q);
   const int64_t slab = static_cast<int64_t>(block_size) * d;
   for (int sub = 0; sub < 8; ++sub) {
     const int64_t after = slab - static_cast<int64_t>(kRowsPerWarp) * d * (sub + 1);
     p->crc_sub[sub] = after >= 0 ? crc_x_pow_bytes(static_cast<uint64_t>(after)) : 0u;
   }
-  p->crc_tail = crc_x_pow_bytes(4);
   p->crc_init = gf2_mul(0xFFFFFFFFu, crc_x_pow_bytes(static_cast<uint64_t>(slab + 4))) ^ 0xFFFFFFFFu;
 }
 
@@ -831,14 +787,9 @@ cudaError_t encode_crc_t(const EncodeParams& p, cudaStream_t s) {
   if (p.B > kRowsPerWarp) {
     k_encode<SrcT, D, 0, true, 0, true><<<p.grid.units, kThreads, 0, s>>>(p);
   } else {
-    constexpr int kPosBytes = EncodeGeom<D>::kPasses * 8 * 256 * 4;
-    auto kern = k_encode<SrcT, D, 0, false, 0, true>;
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPosBytes);
-    if (e != cudaSuccess) return e;
     const uint32_t grid = static_cast<uint32_t>(
         std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * 2));
-    kern<<<grid, kThreads, kPosBytes, s>>>(p);
+    k_encode<SrcT, D, 0, false, 0, true><<<grid, kThreads, 0, s>>>(p);
   }
   return cudaGetLastError();
 }

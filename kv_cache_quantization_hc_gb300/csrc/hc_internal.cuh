@@ -65,11 +65,13 @@ struct EncodeParams {
   // into the encode when crc != null; the constants are built on the host
   // (see encode.cu, "Fused CRC").
   uint32_t* crc;
-  uint32_t crc_kbasis[32];  // x^(8*256) times each single-bit register value
-  uint32_t crc_level[5];    // x^(64 * 2^j): the lanes' butterfly steps
   uint32_t crc_sub[8];      // x^(8 * bytes from sub-slab k's end to the slab's codes' end)
-  uint32_t crc_tail;        // x^(8*4): past the scale bytes
   uint32_t crc_init;        // the initial register's term and the final xor
+  // images of the single-bit inputs of the fused CRC's linear maps
+  uint32_t crc_img_pos[8][64];    // pass i's 8 code bytes -> the lane's register at its last piece
+  uint32_t crc_img_level[5][32];  // a register -> 8 * 2^j bytes later
+  uint32_t crc_img_tail[32];      // a register -> 4 bytes later
+  uint32_t crc_img_scale[32];     // the scale's 4 bytes -> the register after them
 };
 
 struct FetchParams {
@@ -101,15 +103,31 @@ struct TableParams {
 // to the end of the unit by multiplying with lane_shift[k] = x^(8 * bytes
 // after its part) mod P, and init_term adds the initial register's
 // contribution and the final xor.  Constants are built on the host.
+// CRC-32 of units (crc32.cu): rows of 32 16-byte words are taken kCrcGroup
+// at a time, by persistent CTAs, kCrcCtasPerSm per SM.  Measured on GB300 over
+// the Qwen3-8B-shaped FP8 wire (73,728 units of 32 KiB): groups of 4 rows at
+// 8 CTAs/SM 3.43 TB/s; at 4 CTAs/SM 3.17; groups of 8 rows 2.2-2.4.
+#ifndef HC_CRC_GROUP
+#define HC_CRC_GROUP 4
+#endif
+#ifndef HC_CRC_CTAS_PER_SM
+#define HC_CRC_CTAS_PER_SM 8
+#endif
+constexpr int kCrcGroup = HC_CRC_GROUP;
+constexpr int kCrcCtasPerSm = HC_CRC_CTAS_PER_SM;
+
 struct CrcParams {
   const uint8_t* a;
   const uint8_t* b;
   int64_t a_bytes, a_stride, b_bytes, b_stride;
-  int64_t chunk;  // a multiple of 128
   uint32_t n_units;
   uint32_t* crc;
-  uint32_t lane_shift[32];
-  uint32_t init_term;
+  uint32_t seg2_shift;  // x^(8 * bytes of the second segment)
+  uint32_t init_term;   // the initial register's term and the final xor
+  // images of the single-bit inputs of the kernel's linear maps (see crc32.cu)
+  uint32_t img_word[kCrcGroup][128];
+  uint32_t img_group[32];
+  uint32_t img_level[5][32];
 };
 
 // Drift-ranked token selection over n_seq sequences of n_tokens rows of

@@ -119,3 +119,48 @@ def test_fused_slab_crc_matches_the_oracle(d, B, src, ragged, H):
     scales = o["scales"].astype(np.float32).reshape(n, 1).view(np.uint8)
     want = ocrc.crc32_units(codes, codes.shape[1], codes.shape[1], n, scales, 4, 4)
     assert np.array_equal(_u32(crc).reshape(-1), want)
+
+
+@pytest.mark.parametrize("src", ["bf16", "f32"])
+def test_fused_slab_crc_of_a_skipped_block(src):
+    """A block with a bad source slot is flagged and skipped: its wire bytes
+    stay as they were.  For 16-bit sources its CRC entries are not written;
+    for fp32 sources (encode, then the CRC kernel over every slab) they are
+    the CRC of the wire bytes as they stand.  Every other slab's CRC equals
+    the oracle's."""
+    from kv_cache_quantization_hc_gb300 import hc, path as kvpath
+    c = parity.random_case(97, L=2, H=3, d=128, B=16, nb=5, src_fmt=src, out_fmt="bf16")
+    o = parity.oracle_run(c, "fp8")
+    bad = 2
+    slots = c.src_slots.copy()
+    slots[bad] = c.src_k.shape[1] + 5                  # outside [0, num_slots)
+    dm_vals, dm_idx = np.unique(c.delta_m, return_inverse=True)
+    p = kvpath.KVPath(n_layers=c.L, H=c.H, d=c.d, B=c.B, n_blocks=len(slots),
+                      src_slots=slots, dst_slots=c.dst_slots, n_valid=c.n_valid,
+                      delta_m_distinct=dm_vals, delta_idx=dm_idx, wire="fp8", pairing=c.pairing,
+                      rope_base=c.rope_base, paged_dtype="bf16")
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[src]
+    src_k = torch.as_tensor(c.src_k, device=DEV).to(tdt)
+    src_v = torch.as_tensor(c.src_v, device=DEV).to(tdt)
+    p.codes.fill_(0xEE)
+    p.scales.fill_(3.0)
+    crc = torch.full((c.L, len(slots), 2, c.H), 0x5A5A5A5A, dtype=torch.int32, device=DEV)
+    p.encode(src_k, src_v, crc=crc)
+    torch.cuda.synchronize()
+    assert p.error_bits() == hc.HC_DEVERR_SLOT
+    codes = p.codes.cpu().numpy()
+    assert np.all(codes[:, bad] == 0xEE) and torch.all(p.scales[:, bad] == 3.0)
+    keep = [j for j in range(len(slots)) if j != bad]
+    assert np.array_equal(codes[:, keep], o["codes"][:, keep])
+    got = _u32(crc)
+    n_slab = c.B * c.d
+    want = ocrc.crc32_units(o["codes"].reshape(-1, n_slab), n_slab, n_slab, got.size,
+                            o["scales"].astype(np.float32).reshape(-1, 1).view(np.uint8), 4, 4)
+    want = want.reshape(got.shape)
+    assert np.array_equal(got[:, keep], want[:, keep])
+    if src == "f32":
+        stale = ocrc.crc32_units(codes[:, bad].reshape(-1, n_slab), n_slab, n_slab, c.L * 2 * c.H,
+                                 np.full((c.L * 2 * c.H, 1), 3.0, np.float32).view(np.uint8), 4, 4)
+        assert np.array_equal(got[:, bad].reshape(-1), stale)
+    else:
+        assert np.all(got[:, bad] == 0x5A5A5A5A)

@@ -8,8 +8,7 @@ chunks of blocks), plus properties that hold at any size.
   layers, all 2048 blocks each, are compared with the oracle.
 * llama3_70b: 80 layers fetched one layer per call on a side stream into a
   bf16 paged cache, after per-layer encodes on the main stream; every block
-  of the first, a middle and the last layer is compared with the oracle, and
-  every slot of every layer is checked written.
+  of all 80 layers is compared with the oracle.
 * ragged: 36 layers, block sizes 16 and 64 in separate calls, ragged tails,
   INT4 (g32, fp16 scales) and FP8; every block (both block sizes, every
   padding row) of the first, a middle and the last layer is compared with
@@ -134,7 +133,7 @@ def test_llama3_70b_layer_streamed(pool):
     assert not torch.isnan(dst_k).any() and not torch.isnan(dst_v).any()
     # distinct delta-m values: one table row each, shared by all 80 layers
     assert p.n_distinct == len(np.unique(blk.delta_m)) <= 1024
-    layers = [0, w.L // 2, w.L - 1]
+    layers = range(w.L)
     for layer in layers:
         k = workloads.device_pool(w, blk, range(layer, layer + 1), 0, dev)[0]
         v = workloads.device_pool(w, blk, range(layer, layer + 1), 1, dev)[0]
