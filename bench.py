@@ -327,6 +327,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "tokens_per_s": total_tokens / max_s,
             "hbm_frac": total_bytes / max_s / 1e9 / world / peak,
+            "hbm_frac_nominal": total_bytes / max_s / 1e9 / world / NOMINAL_HBM_GBS,
             "kernels": kern,
             "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak,

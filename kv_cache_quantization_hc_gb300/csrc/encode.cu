@@ -635,9 +635,10 @@ __global__ void __launch_bounds__(kThreads, HC_ENCODE_WIDE_MIN_BLOCKS) k_encode_
 // kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
 // kCrc: the FP8 wire with the fused slab CRC (16-bit sources).
 template <typename SrcT, int D, int kWire, bool kFlat, int kGroupLog2, bool kCrc = false>
-__global__ void __launch_bounds__(kThreads, kFlat ? 4 : 2) k_encode(const __grid_constant__ EncodeParams p) {
+__global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerSm > 2)) ? 4 : 2)
+    k_encode(const __grid_constant__ EncodeParams p) {
   using G = EncodeGeom<D>;
-  constexpr bool kDoubleBuffer = !kFlat && sizeof(SrcT) == 2;
+  constexpr bool kDoubleBuffer = !kFlat && sizeof(SrcT) == 2 && !(kCrc && kFusedCrcCtasPerSm > 2);
   static_assert(!kCrc || (kWire == 0 && sizeof(SrcT) == 2), "fused CRC: FP8, 16-bit sources");
   __shared__ float s_amax[2][kWarps];
   __shared__ uint32_t s_crc[2][kWarps];
@@ -788,7 +789,7 @@ cudaError_t encode_crc_t(const EncodeParams& p, cudaStream_t s) {
     k_encode<SrcT, D, 0, true, 0, true><<<p.grid.units, kThreads, 0, s>>>(p);
   } else {
     const uint32_t grid = static_cast<uint32_t>(
-        std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * 2));
+        std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * kFusedCrcCtasPerSm));
     k_encode<SrcT, D, 0, false, 0, true><<<grid, kThreads, 0, s>>>(p);
   }
   return cudaGetLastError();

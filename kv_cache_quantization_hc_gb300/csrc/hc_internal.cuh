@@ -115,6 +115,14 @@ struct TableParams {
 #endif
 constexpr int kCrcGroup = HC_CRC_GROUP;
 constexpr int kCrcCtasPerSm = HC_CRC_CTAS_PER_SM;
+// The encoder's fused slab CRC with 16-token blocks: persistent CTAs, 2 per
+// SM with the per-warp double buffer (128 registers), or 3-4 per SM with a
+// single buffer (64 registers).  Measured on the Qwen3-8B-shaped encode:
+// 1.66 ms (2), 1.67 ms (3), 1.63 ms (4); the plain encode takes 1.08 ms.
+#ifndef HC_FUSED_CRC_CTAS_PER_SM
+#define HC_FUSED_CRC_CTAS_PER_SM 4
+#endif
+constexpr int kFusedCrcCtasPerSm = HC_FUSED_CRC_CTAS_PER_SM;
 
 struct CrcParams {
   const uint8_t* a;
