@@ -247,7 +247,11 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
  *   a        : device, 16-byte aligned; a_stride a multiple of 16; a_bytes >= 0
  *   b        : device, any alignment, or NULL when b_bytes == 0
  *   n_units  : >= 0; 0 launches nothing
- *   crc      : device u32 [n_units], written in full
+ *   crc      : device u32 [n_units], written in full.  When there are few,
+ *              large units (each is then cut into chunks across warps), the
+ *              call first zeroes crc[] on `stream` and the chunks' terms are
+ *              xor-ed into it; a concurrent reader of crc[] sees partial
+ *              values until the call's work completes.
  * Returns HC_OK, HC_ERR_INVALID_ARG or HC_ERR_CUDA. */
 int hc_crc32(const void* a, int64_t a_bytes, int64_t a_stride, const void* b, int64_t b_bytes,
              int64_t b_stride, int32_t n_units, uint32_t* crc, void* stream);

@@ -74,31 +74,50 @@ __device__ __forceinline__ uint32_t word_contrib(const FieldMap<128>& m, uint4 w
   return apply_map<128>(m, v);
 }
 
-// Segment 1: the n_words 16-byte words at `a`.  Only the first group can
-// hold front padding; the rest read at a pointer that steps a group at a time.
-__device__ __forceinline__ uint32_t aligned_segment(const CrcShared& s, const uint4* a,
-                                                    int64_t n_words, int lane) {
+// The lane's register over groups [g0, g1) of segment 1 (the 16-byte words
+// at `a`, front-padded to whole groups), positioned at the end of its last
+// word in group g1 - 1.  `first` is the word index of this lane's word in
+// row 0 of group 0 (negative in the padding).  Only group 0 can hold front
+// padding; the rest read at a pointer that steps a group at a time.
+__device__ __forceinline__ uint32_t group_range(const CrcShared& s, const uint4* a, int64_t first,
+                                                int64_t g0, int64_t g1) {
   constexpr int kGroupWords = 32 * kCrcGroup;
-  const int groups = static_cast<int>((n_words + kGroupWords - 1) / kGroupWords);
-  const int64_t first = n_words - static_cast<int64_t>(groups) * kGroupWords + lane;  // > lane - 128
   uint32_t r = 0;
+  int64_t g = g0;
+  if (g == 0 && g < g1) {
 #pragma unroll
-  for (int g = 0; g < kCrcGroup; ++g) {
-    const int64_t k = first + g * 32;
-    r ^= word_contrib(s.word[g], k >= 0 ? __ldcs(a + k) : make_uint4(0u, 0u, 0u, 0u));
+    for (int j = 0; j < kCrcGroup; ++j) {
+      const int64_t k = first + j * 32;
+      r ^= word_contrib(s.word[j], k >= 0 ? __ldcs(a + k) : make_uint4(0u, 0u, 0u, 0u));
+    }
+    ++g;
   }
-  const uint4* ptr = a + (first + kGroupWords);
+  if (g >= g1) return r;
+  const uint4* ptr = a + (first + g * kGroupWords);
+  const int n = static_cast<int>(g1 - g);
 #pragma unroll 2
-  for (int gi = 1; gi < groups; ++gi, ptr += kGroupWords) {
+  for (int gi = 0; gi < n; ++gi, ptr += kGroupWords) {
     uint4 w[kCrcGroup];
 #pragma unroll
-    for (int g = 0; g < kCrcGroup; ++g) w[g] = __ldcs(ptr + g * 32);
+    for (int j = 0; j < kCrcGroup; ++j) w[j] = __ldcs(ptr + j * 32);
     uint32_t c = apply_map(s.group, r);
 #pragma unroll
-    for (int g = 0; g < kCrcGroup; ++g) c ^= word_contrib(s.word[g], w[g]);
+    for (int j = 0; j < kCrcGroup; ++j) c ^= word_contrib(s.word[j], w[j]);
     r = c;
   }
-  return lane_tree(s, r, lane);
+  return r;
+}
+
+__device__ __forceinline__ int64_t padded_groups(int64_t n_words) {
+  return (n_words + 32 * kCrcGroup - 1) / (32 * kCrcGroup);
+}
+
+// Segment 1 of a unit: lane 0 ends with its register at the segment's end.
+__device__ __forceinline__ uint32_t aligned_segment(const CrcShared& s, const uint4* a,
+                                                    int64_t n_words, int lane) {
+  const int64_t groups = padded_groups(n_words);
+  const int64_t first = n_words - groups * 32 * kCrcGroup + lane;  // > lane - 128
+  return lane_tree(s, group_range(s, a, first, 0, groups), lane);
 }
 
 // Segment 2: t bytes at `at`, then nb bytes at `b`, read byte by byte.
@@ -147,6 +166,46 @@ __global__ void __launch_bounds__(kThreads) k_crc32(const __grid_constant__ CrcP
   }
 }
 
+// Few, large units: each unit's segment 1 is cut into chunks of
+// p.chunk_groups groups, one warp per chunk, and one more warp per unit takes
+// segment 2.  A chunk's register is moved to the unit's end (past the rest of
+// segment 1 and all of segment 2) and xor-ed into crc[u], which the host
+// zeroed; the segment-2 warp adds the initial register's term and the final
+// xor.  The xors commute, so the result does not depend on their order.
+__global__ void __launch_bounds__(kThreads) k_crc32_split(const __grid_constant__ CrcParams p) {
+  __shared__ CrcShared maps;
+  build_maps(p, maps);
+  const int lane = threadIdx.x & 31;
+  const int64_t words = p.a_bytes >> 4, t = p.a_bytes & 15;
+  const int64_t groups = padded_groups(words);
+  const int64_t per_unit = p.chunks + 1;  // chunk warps, then the segment-2 warp
+  const int64_t total = per_unit * p.n_units;
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); item < total;
+       item += static_cast<int64_t>(gridDim.x) * kWarps) {
+    const int64_t u = item / per_unit, k = item % per_unit;
+    const uint8_t* a = p.a + u * p.a_stride;
+    uint32_t r;
+    if (k < p.chunks) {
+      const int64_t g0 = k * p.chunk_groups;
+      const int64_t g1 = g0 + p.chunk_groups < groups ? g0 + p.chunk_groups : groups;
+      const int64_t first = words - groups * 32 * kCrcGroup + lane;
+      r = lane_tree(maps, group_range(maps, reinterpret_cast<const uint4*>(a), first, g0, g1), lane);
+      if (lane == 0) {
+        // x^(8 * 16 * 32 * kCrcGroup * (groups - g1)) from the host's powers of two
+        uint32_t m = 0x80000000u;
+        for (int64_t e = groups - g1, i = 0; e; e >>= 1, ++i)
+          if (e & 1) m = gf2_mul(m, p.group_pow2[i]);
+        r = gf2_mul(gf2_mul(r, m), p.seg2_shift);
+      }
+    } else {
+      const uint8_t* b = p.b_bytes > 0 ? p.b + u * p.b_stride : nullptr;
+      r = t + p.b_bytes > 0 ? byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane) : 0u;
+      r ^= p.init_term;
+    }
+    if (lane == 0) atomicXor(p.crc + u, r);
+  }
+}
+
 // The images of the maps' single-bit inputs; they depend on nothing but the
 // polynomial and kCrcGroup, so they are computed once per process.
 struct CrcImages {
@@ -186,10 +245,26 @@ cudaError_t launch_crc32(const CrcParams& in, cudaStream_t s) {
   const uint64_t n = static_cast<uint64_t>(p.a_bytes + p.b_bytes);
   p.seg2_shift = crc_x_pow_bytes(static_cast<uint64_t>((p.a_bytes & 15) + p.b_bytes));
   p.init_term = gf2_mul(0xFFFFFFFFu, crc_x_pow_bytes(n)) ^ 0xFFFFFFFFu;
-  const int64_t ctas = (static_cast<int64_t>(p.n_units) + kWarps - 1) / kWarps;
-  const uint32_t grid = static_cast<uint32_t>(
-      std::min<int64_t>(ctas, static_cast<int64_t>(device_sm_count()) * kCrcCtasPerSm));
-  k_crc32<<<grid, kThreads, 0, s>>>(p);
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) * kCrcCtasPerSm;
+  const int64_t groups = (p.a_bytes / 16 + 32 * kCrcGroup - 1) / (32 * kCrcGroup);
+  if (static_cast<int64_t>(p.n_units) * 2 >= resident * kWarps || groups < 2 * kCrcMinChunkGroups) {
+    // one warp per unit
+    const int64_t ctas = (static_cast<int64_t>(p.n_units) + kWarps - 1) / kWarps;
+    k_crc32<<<static_cast<uint32_t>(std::min<int64_t>(ctas, resident)), kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+  }
+  // few, large units: chunks of at least kCrcMinChunkGroups groups, about
+  // two warps' worth per resident warp slot
+  const int64_t want = std::max<int64_t>(1, 2 * resident * kWarps / p.n_units);
+  p.chunk_groups = std::max<int64_t>(kCrcMinChunkGroups, (groups + want - 1) / want);
+  p.chunks = (groups + p.chunk_groups - 1) / p.chunk_groups;
+  for (int i = 0; i < 48; ++i)
+    p.group_pow2[i] = crc_x_pow_bytes((16ull * 32 * kCrcGroup) << i);
+  const cudaError_t e = cudaMemsetAsync(p.crc, 0, sizeof(uint32_t) * p.n_units, s);
+  if (e != cudaSuccess) return e;
+  const int64_t warps = (p.chunks + 1) * static_cast<int64_t>(p.n_units);
+  const int64_t ctas = (warps + kWarps - 1) / kWarps;
+  k_crc32_split<<<static_cast<uint32_t>(std::min<int64_t>(ctas, resident)), kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -115,6 +115,9 @@ struct TableParams {
 #endif
 constexpr int kCrcGroup = HC_CRC_GROUP;
 constexpr int kCrcCtasPerSm = HC_CRC_CTAS_PER_SM;
+// Units too few to fill the GPU one warp each are cut into chunks of at least
+// this many groups (64 groups of 2 KiB: 128 KiB).
+constexpr int kCrcMinChunkGroups = 64;
 // The encoder's fused slab CRC with 16-token blocks: persistent CTAs, 2 per
 // SM with the per-warp double buffer (128 registers), or 3-4 per SM with a
 // single buffer (64 registers).  Measured on the Qwen3-8B-shaped encode:
@@ -132,6 +135,10 @@ struct CrcParams {
   uint32_t* crc;
   uint32_t seg2_shift;  // x^(8 * bytes of the second segment)
   uint32_t init_term;   // the initial register's term and the final xor
+  // split launch (few, large units): chunks per unit, groups per chunk, and
+  // x^(8 * bytes of 2^i groups)
+  int64_t chunks, chunk_groups;
+  uint32_t group_pow2[48];
   // images of the single-bit inputs of the kernel's linear maps (see crc32.cu)
   uint32_t img_word[kCrcGroup][128];
   uint32_t img_group[32];

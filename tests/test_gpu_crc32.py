@@ -1,6 +1,8 @@
 """GPU parity of the CRC-32 kernel (hc_crc32) against the oracle's CRC-32,
-on random units of many sizes and on encoded wire buffers, plus tamper
-detection: changing one byte of a unit changes that unit's CRC only."""
+on random units of many sizes (many small units, one warp each; and a few
+units of up to 64 MiB, which the library cuts into chunks across warps) and
+on encoded wire buffers, plus tamper detection: changing one byte of a unit
+changes that unit's CRC only."""
 import numpy as np
 import pytest
 import torch
@@ -26,7 +28,10 @@ def _u32(t):
 SHAPES = [(0, 0, 0, 0, 3), (0, 16, 5, 7, 4), (1, 16, 0, 0, 5), (15, 16, 3, 3, 2),
           (16, 32, 0, 0, 9), (4095, 4096, 1, 1, 3), (4096, 4096, 64, 64, 17),
           (4096 + 48, 4160, 13, 20, 6), (32768, 32768, 64, 64, 40), (65536 + 16, 65552, 0, 0, 3),
-          (131072, 131072, 2048, 2048, 2)]
+          (131072, 131072, 2048, 2048, 2),
+          # few, large units: each unit is cut into chunks across warps
+          (262144 + 3, 262160, 0, 0, 1), (1 << 20, 1 << 20, 0, 0, 5),
+          (8 * 2 ** 20 + 4100, 8 * 2 ** 20 + 4112, 77, 80, 3), (64 * 2 ** 20 + 5, 64 * 2 ** 20 + 16, 13, 13, 1)]
 
 
 @pytest.mark.parametrize("a_bytes,a_stride,b_bytes,b_stride,n", SHAPES)
