@@ -31,9 +31,10 @@
 // second segment and adds the second's, the initial register's term and the
 // final xor.
 //
-// Why rows: the previous design gave each lane a contiguous piece of the unit,
-// so a warp's 16-byte loads touched 32 lines 1 KiB apart; that layout, plus
-// byte-indexed tables whose lookups collide, held the kernel to 2.0 TB/s.
+// Why rows: giving each lane a contiguous piece of the unit instead (as a first
+// design did) makes a warp's 16-byte loads touch 32 lines 1 KiB apart; that
+// layout, with byte-indexed tables whose lookups collide, held the kernel to
+// 2.0 TB/s.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
