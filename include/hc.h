@@ -18,7 +18,8 @@
  *   current CUDA device can access; every call enqueues work on `stream`
  *   (a cudaStream_t; NULL = the legacy default stream) and returns without
  *   synchronizing.  The library allocates, frees and synchronizes nothing and
- *   keeps no global state; calls are thread-safe.
+ *   keeps no mutable global state (only constants computed once per process);
+ *   calls are thread-safe.
  * - Host-side argument errors return a negative hc_status synchronously and
  *   launch nothing.  A failed launch returns HC_ERR_CUDA.
  * - Data errors found on the device (a slot id outside [0, num_slots), a
