@@ -14,14 +14,15 @@
 // into pieces whose registers are computed independently and moved to the
 // message's end by multiplying with x^(8 * bytes after the piece).
 //
-// One warp per unit, persistent CTAs.  A unit is two segments: the 16-byte
+// One warp per unit, persistent CTAs (k_crc32); few, large units are cut
+// into chunks across warps (k_crc32_split, below).  A unit is two segments: the 16-byte
 // words of a (16-byte aligned), then the ragged rest of a followed by b, read
 // byte by byte and padded in front with zero bytes to whole 16-byte words
 // (leading zeros leave a zero-started register unchanged).  A segment is cut
 // into rows of 32 words, 512 bytes, and padded in front with zero words to a
-// whole number of groups of kGroup rows.  Lane l takes word l of every row, so
+// whole number of groups of kCrcGroup rows.  Lane l takes word l of every row, so
 // a warp's loads are 512 contiguous bytes.  Per group of rows a lane moves its
-// register past the group (x^(8 * 512 * kGroup)) and adds each of its words'
+// register past the group (x^(8 * 512 * kCrcGroup)) and adds each of its words'
 // contributions, read from the map of that word's row position; the register
 // then describes everything the lane has read, with every other lane's bytes
 // taken as zero, positioned at the end of the lane's last word.  A butterfly
@@ -49,7 +50,7 @@ namespace {
 // Tables of one CTA, filled from the host-computed images in CrcParams.
 struct CrcShared {
   FieldMap<128> word[kCrcGroup];  // word at row position g of a group -> register at the group's end
-  FieldMap<32> group;             // a register -> the register kGroup rows later
+  FieldMap<32> group;             // a register -> the register kCrcGroup rows later
   FieldMap<32> level[5];          // a register -> the register 16 * 2^j bytes later
 };
 
