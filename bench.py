@@ -13,6 +13,10 @@ the whole job (all ranks), with inputs resident in HBM; `e2e` is the same
 metric with the source copied from pinned host memory and the result copied
 back inside the timed region; `cpu_baseline` / `--impl reference` time the
 float64 oracle on the host cores on a bounded sample of the same workload.
+`workloads` adds the two per-layer workloads, each call timed with CUDA
+events: the Llama-3-70B-shaped layer-streamed fetch (80 layers, FP8, against
+70% of the nominal 8 TB/s per layer) and the ragged INT4 sweep (36 layers,
+blocks of 16 and 64); these run after the step's own timed region.
 Under torchrun each rank runs an independent replica (weak scaling: the path
 has no exchange step).
 """
