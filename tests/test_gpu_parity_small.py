@@ -207,9 +207,13 @@ def test_device_error_flag_encode_skips_block(bad, bit):
     assert np.array_equal(codes[:, [0, 1, 3]], want)
 
 
+@pytest.mark.parametrize("wire", ["fp8", "int4"])
 @pytest.mark.parametrize("bad,bit", [("slot", 1), ("delta", 2), ("nvalid", 4)])
-def test_device_error_flag_fetch_skips_block(bad, bit):
-    c, p, k, v = _tiny_path()
+def test_device_error_flag_fetch_skips_block(bad, bit, wire):
+    """A bad destination slot, delta-m index or n_valid flags its bit and skips
+    the block's K and V; every other block is written.  The INT4 fetch takes K
+    and V of a sub-slab in one warp, so both are checked there too."""
+    c, p, k, v = _tiny_path(wire)
     p.encode(k, v)
     p.build_table()
     if bad == "slot":
@@ -223,11 +227,13 @@ def test_device_error_flag_fetch_skips_block(bad, bit):
     p.fetch(dk, dv)
     torch.cuda.synchronize()
     assert p.error_bits() == bit
-    if bad != "slot":
-        assert torch.all(dk[0, c.dst_slots[1]] == parity.SENTINEL)
-        assert torch.all(dv[0, c.dst_slots[1]] == parity.SENTINEL)
-    for j in (0, 2, 3):
-        assert not torch.any(dk[0, c.dst_slots[j]] == parity.SENTINEL)
+    good = {int(c.dst_slots[j]) for j in (0, 2, 3)}
+    for slot in range(c.num_dst_slots):   # the bad block's slot and unused slots keep the sentinel
+        for t in (dk, dv):
+            if slot in good:
+                assert not torch.any(t[0, slot] == parity.SENTINEL)
+            else:
+                assert torch.all(t[0, slot] == parity.SENTINEL)
 
 
 def test_empty_call_is_a_no_op():
