@@ -246,7 +246,10 @@ int hc_fetch_rotate_scatter(int32_t wire, const void* codes, const void* scales,
  *  (.hckv + CRC32)", and the CRC32 tamper-detection tests it lists.]
  *
  *   a        : device, 16-byte aligned; a_stride a multiple of 16; a_bytes >= 0
- *   b        : device, any alignment, or NULL when b_bytes == 0
+ *   b        : device, any alignment, or NULL when b_bytes == 0.  b (and the
+ *              last a_bytes % 16 bytes of a) is read byte by byte by one warp
+ *              per unit: meant for a short trailer such as the scales; the
+ *              16-byte words of a are read at full speed
  *   n_units  : >= 0; 0 launches nothing
  *   crc      : device u32 [n_units], written in full.  When there are few,
  *              large units (each is then cut into chunks across warps), the
