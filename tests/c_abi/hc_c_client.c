@@ -8,7 +8,9 @@
  * src_slots[nb], dst_slots[nb], n_valid[nb], delta_idx[nb];
  * int32 delta_m[n_distinct]; float32 dst_init[L][S_dst][B][H][d].
  * Output: u8 codes[L][nb][2][H][B][d]; f32 scales[L][nb][2][H];
- * f32 out_k[L][S_dst][B][H][d], out_v[...]; int32 err.
+ * f32 out_k[L][S_dst][B][H][d], out_v[...]; int32 err; u32 crc[L][nb] (the
+ * CRC-32 of each (layer, block)'s codes followed by its scales); int32
+ * hc_selection_size(1408).
  * Usage: hc_c_client <in> <out>; exit status 0 on success. */
 #include <stdint.h>
 #include <stdio.h>
@@ -67,9 +69,10 @@ int main(int argc, char** argv) {
   void *d_nv = to_device(h_nv, (size_t)nb * 4), *d_di = to_device(h_di, (size_t)nb * 4);
   void* d_dm = to_device(h_dm, (size_t)nd * 4);
   void *d_ok = to_device(h_init, dst_elems * 4), *d_ov = to_device(h_init, dst_elems * 4);
-  void *d_codes = NULL, *d_scales = NULL, *d_table = NULL, *d_err = NULL;
+  void *d_codes = NULL, *d_scales = NULL, *d_table = NULL, *d_err = NULL, *d_crc = NULL;
   if (cudaMalloc(&d_codes, n_codes) || cudaMalloc(&d_scales, n_scales * 4) ||
-      cudaMalloc(&d_table, (size_t)nd * d * 4) || cudaMalloc(&d_err, 4) || cudaMemset(d_err, 0, 4))
+      cudaMalloc(&d_table, (size_t)nd * d * 4) || cudaMalloc(&d_err, 4) || cudaMemset(d_err, 0, 4) ||
+      cudaMalloc(&d_crc, (size_t)L * nb * 4))
     return 3;
 
   hc_paged_desc src = {L, H, d, B, S_src, HC_F16, (int64_t)B * H * d, (int64_t)S_src * B * H * d};
@@ -82,6 +85,11 @@ int main(int argc, char** argv) {
         hc_fetch_rotate_scatter(HC_WIRE_FP8, d_codes, d_scales, 32, HC_F16, (const float*)d_table,
                                 (const int32_t*)d_di, nd, HC_PAIR_HALF_SPLIT, (const int32_t*)d_dst,
                                 (const int32_t*)d_nv, nb, d_ok, d_ov, &dst, (int32_t*)d_err, NULL));
+  {
+    const int64_t unit_codes = (int64_t)2 * H * B * d, unit_scales = (int64_t)2 * H * 4;
+    check("hc_crc32", hc_crc32(d_codes, unit_codes, unit_codes, d_scales, unit_scales, unit_scales,
+                               L * nb, (uint32_t*)d_crc, NULL));
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) return 5;
 
   uint8_t* codes = (uint8_t*)malloc(n_codes);
@@ -89,7 +97,9 @@ int main(int argc, char** argv) {
   float* ok = (float*)malloc(dst_elems * 4);
   float* ov = (float*)malloc(dst_elems * 4);
   int32_t err = -1;
-  if (cudaMemcpy(codes, d_codes, n_codes, cudaMemcpyDeviceToHost) ||
+  uint32_t* crc = (uint32_t*)malloc((size_t)L * nb * 4);
+  if (cudaMemcpy(crc, d_crc, (size_t)L * nb * 4, cudaMemcpyDeviceToHost) ||
+      cudaMemcpy(codes, d_codes, n_codes, cudaMemcpyDeviceToHost) ||
       cudaMemcpy(scales, d_scales, n_scales * 4, cudaMemcpyDeviceToHost) ||
       cudaMemcpy(ok, d_ok, dst_elems * 4, cudaMemcpyDeviceToHost) ||
       cudaMemcpy(ov, d_ov, dst_elems * 4, cudaMemcpyDeviceToHost) ||
@@ -102,6 +112,9 @@ int main(int argc, char** argv) {
   fwrite(ok, 4, dst_elems, o);
   fwrite(ov, 4, dst_elems, o);
   fwrite(&err, 4, 1, o);
+  fwrite(crc, 4, (size_t)L * nb, o);
+  const int32_t k_default = hc_selection_size(1408);
+  fwrite(&k_default, 4, 1, o);
   fclose(o);
   printf("hc_c_client: ok (library API version %d)\n", hc_version());
   return 0;

@@ -1,6 +1,7 @@
 """The C ABI from plain C: a C program (tests/c_abi/hc_c_client.c), compiled
-against include/hc.h and linked to libhc.so, runs encode, table and fetch on
-cudaMalloc'd buffers; its outputs are compared with the oracle."""
+against include/hc.h and linked to libhc.so, runs encode, table, fetch and
+the CRC-32 of the wire on cudaMalloc'd buffers, and asks for the default
+selection size; its outputs are compared with the oracle."""
 import os
 import shutil
 import subprocess
@@ -62,6 +63,11 @@ def test_c_client_matches_the_oracle(client, tmp_path):
     v = raw[o:o + 4 * n_dst].view("<f4").reshape(L, S_dst, B, H, d)
     o += 4 * n_dst
     err = int(raw[o:o + 4].view("<i4")[0])
+    o += 4
+    crc = raw[o:o + 4 * L * nb].view("<u4")
+    o += 4 * L * nb
+    k_default = int(raw[o:o + 4].view("<i4")[0])
+    assert o + 4 == raw.size
     want = parity.oracle_run(c, "fp8")
     assert err == 0
     assert np.array_equal(codes, want["codes"])
@@ -69,3 +75,9 @@ def test_c_client_matches_the_oracle(client, tmp_path):
     rep = parity.compare_outputs(c, "fp8", {"k": k.astype(np.float64), "v": v.astype(np.float64)},
                                  want)
     assert rep["k_ok"] and rep["v_ok"] and rep["k_untouched_ok"] and rep["v_untouched_ok"], rep
+    from oracle import blend, crc32 as ocrc
+    a = want["codes"].reshape(L * nb, -1)
+    b = want["scales"].astype("<f4").reshape(L * nb, -1).view(np.uint8)
+    assert np.array_equal(crc, ocrc.crc32_units(a, a.shape[1], a.shape[1], L * nb, b, b.shape[1],
+                                                b.shape[1]))
+    assert k_default == blend.default_k(1408) == 212
