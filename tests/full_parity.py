@@ -82,7 +82,7 @@ def check_chunk(t):
     m = np.zeros((1, n, B), bool)
     m[0] = np.arange(B)[None, :] < nv[:, None]
     res["k_ok"], res["k_max_err"], res["k_bar"] = compare_k(gk[m], ek[m], t["out_fmt"])
-    res["v_ok"], res["v_exact"] = compare_v(gv[m], ev[m], wire, t["out_fmt"])
+    res["v_ok"], res["v_exact"] = compare_v(gv[m], ev[m], wire, t["out_fmt"], t["scale_dtype"])
     # padding rows of ragged blocks: never written, so still the sentinel
     res["padding_ok"] = bool(np.array_equal(gk[~m], ek[~m]) and np.array_equal(gv[~m], ev[~m]))
     res["ok"] = all(res[x] for x in ("codes_ok", "scales_ok", "k_ok", "v_ok", "padding_ok"))

@@ -9,9 +9,9 @@ the C ABI, to the CUDA path, and compares:
 * fetched K: fp32 output within 2e-6 x the row's max |k|; fp16/bf16 output
   within 1 ulp of the larger of the two values, plus the same 2e-6 x row-max
   floor (below it the fp32 rotation's own rounding decides the last bit);
-* fetched V: bit-exact, except FP8-sourced V (either FP8 wire) rounded to
-  fp16/bf16, where the fp32 dequantized value is rounded a second time
-  (within 1 ulp);
+* fetched V: bit-exact, except where the fp32 dequantized value is rounded
+  a second time to fp16/bf16 (FP8-sourced V, and INT4 with fp32 scales;
+  within 1 ulp);
 * every element the fetch must not touch keeps its sentinel, bit for bit.
 """
 from dataclasses import dataclass
@@ -143,7 +143,7 @@ def written_mask(c):
     return m
 
 
-def compare_outputs(c, wire, gout, oout):
+def compare_outputs(c, wire, gout, oout, scale_dtype="f16"):
     rep = {}
     m = written_mask(c)
     for name in ("k", "v"):
@@ -151,7 +151,7 @@ def compare_outputs(c, wire, gout, oout):
         rep[f"{name}_untouched_ok"] = bool(untouched_ok)
     ok_k, kerr, kbar = compare_k(gout["k"][m], oout["k"][m], c.out_fmt)
     rep.update(k_ok=ok_k, k_max_err=kerr, k_bar=kbar)
-    rep["v_ok"], rep["v_exact"] = compare_v(gout["v"][m], oout["v"][m], wire, c.out_fmt)
+    rep["v_ok"], rep["v_exact"] = compare_v(gout["v"][m], oout["v"][m], wire, c.out_fmt, scale_dtype)
     return rep
 
 
@@ -170,7 +170,7 @@ def run_case(c, wire, group=32, scale_dtype="f16", device="cuda"):
     t_ulp = ulp(o["table"], "f32")
     rep["table_ok"] = bool(np.all(np.abs(g["table"] - o["table"]) <= t_ulp))
     rep["table_exact"] = bool(np.array_equal(g["table"], o["table"]))
-    rep.update(compare_outputs(c, wire, g, o))
+    rep.update(compare_outputs(c, wire, g, o, scale_dtype))
     rep["ok"] = (rep["err"] == 0 and rep.get("codes_exact", True) and rep.get("scales_exact", True)
                  and rep["table_ok"] and rep["k_ok"] and rep["v_ok"]
                  and rep["k_untouched_ok"] and rep["v_untouched_ok"])

@@ -1,8 +1,9 @@
 """GPU parity on the small workloads and a sweep of shapes, through the C ABI.
 
 Bars (tests/parity.py): codes/scales bit-exact; K within 2e-6 x row max
-(fp32) or 1 ulp (+ that floor) for fp16/bf16; V bit-exact (1 ulp for FP8 into
-16-bit outputs); untouched destination bytes unchanged.
+(fp32) or 1 ulp (+ that floor) for fp16/bf16; V bit-exact (1 ulp for FP8, and
+INT4 with fp32 scales, into 16-bit outputs); untouched destination bytes
+unchanged.
 """
 import zlib
 
