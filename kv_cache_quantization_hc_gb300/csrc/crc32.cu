@@ -18,7 +18,9 @@
 // into chunks across warps (k_crc32_split, below).  A unit is two segments: the 16-byte
 // words of a (16-byte aligned), then the ragged rest of a followed by b, read
 // byte by byte and padded in front with zero bytes to whole 16-byte words
-// (leading zeros leave a zero-started register unchanged).  A segment is cut
+// (leading zeros leave a zero-started register unchanged).  Where a has no
+// ragged rest and b is whole 16-byte words on 16-byte boundaries (the FP8
+// wire's scales), the second segment is read as words too.  A segment is cut
 // into rows of 32 words, 512 bytes, and padded in front with zero words to a
 // whole number of groups of kCrcGroup rows.  Lane l takes word l of every row, so
 // a warp's loads are 512 contiguous bytes.  Per group of rows a lane moves its
@@ -76,19 +78,27 @@ __device__ __forceinline__ uint32_t word_contrib(const FieldMap<128>& m, uint4 w
   return apply_map<128>(m, v);
 }
 
-// The lane's register over groups [g0, g1) of segment 1 (the 16-byte words
-// at `a`, front-padded to whole groups), positioned at the end of its last
-// word in group g1 - 1.  `first` is the word index of this lane's word in
-// row 0 of group 0 (negative in the padding).  Only group 0 can hold front
+// Whether row j of a segment's first group holds any word (rows wholly in
+// the front padding contribute nothing and are skipped).  `first0` is the
+// word index of lane 0's word in row 0, the same in every lane.
+__device__ __forceinline__ bool row_has_words(int64_t first0, int j) {
+  return first0 + 31 + 32 * j >= 0;
+}
+
+// The lane's register over groups [g0, g1) of a segment of 16-byte words at
+// `a` (front-padded to whole groups), positioned at the end of its last word
+// in group g1 - 1.  `first` is the word index of this lane's word in row 0
+// of group 0 (negative in the padding).  Only group 0 can hold front
 // padding; the rest read at a pointer that steps a group at a time.
 __device__ __forceinline__ uint32_t group_range(const CrcShared& s, const uint4* a, int64_t first,
-                                                int64_t g0, int64_t g1) {
+                                                int lane, int64_t g0, int64_t g1) {
   constexpr int kGroupWords = 32 * kCrcGroup;
   uint32_t r = 0;
   int64_t g = g0;
   if (g == 0 && g < g1) {
 #pragma unroll
     for (int j = 0; j < kCrcGroup; ++j) {
+      if (!row_has_words(first - lane, j)) continue;
       const int64_t k = first + j * 32;
       r ^= word_contrib(s.word[j], k >= 0 ? __ldcs(a + k) : make_uint4(0u, 0u, 0u, 0u));
     }
@@ -114,12 +124,13 @@ __device__ __forceinline__ int64_t padded_groups(int64_t n_words) {
   return (n_words + 32 * kCrcGroup - 1) / (32 * kCrcGroup);
 }
 
-// Segment 1 of a unit: lane 0 ends with its register at the segment's end.
+// A segment of n_words 16-byte words: lane 0 ends with its register at the
+// segment's end.
 __device__ __forceinline__ uint32_t aligned_segment(const CrcShared& s, const uint4* a,
                                                     int64_t n_words, int lane) {
   const int64_t groups = padded_groups(n_words);
   const int64_t first = n_words - groups * 32 * kCrcGroup + lane;  // > lane - 128
-  return lane_tree(s, group_range(s, a, first, 0, groups), lane);
+  return lane_tree(s, group_range(s, a, first, lane, 0, groups), lane);
 }
 
 // Segment 2: t bytes at `at`, then nb bytes at `b`, read byte by byte.
@@ -132,9 +143,10 @@ __device__ __forceinline__ uint32_t byte_segment(const CrcShared& s, const uint8
   const int64_t first = n_words - groups * 32 * kCrcGroup + lane;
   uint32_t r = 0;
   for (int64_t gi = 0; gi < groups; ++gi) {
-    uint32_t c = apply_map(s.group, r);
+    uint32_t c = gi ? apply_map(s.group, r) : 0u;
 #pragma unroll
     for (int g = 0; g < kCrcGroup; ++g) {
+      if (gi == 0 && !row_has_words(first - lane, g)) continue;
       const int64_t k = first + (gi * kCrcGroup + g) * 32;
       uint32_t v[4] = {0u, 0u, 0u, 0u};
       if (k >= 0) {
@@ -162,7 +174,8 @@ __global__ void __launch_bounds__(kThreads) k_crc32(const __grid_constant__ CrcP
     uint32_t r2 = 0;
     if (t + p.b_bytes > 0) {
       const uint8_t* b = p.b_bytes > 0 ? p.b + static_cast<int64_t>(u) * p.b_stride : nullptr;
-      r2 = byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane);
+      r2 = p.b_words ? aligned_segment(maps, reinterpret_cast<const uint4*>(b), p.b_bytes >> 4, lane)
+                     : byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane);
     }
     if (lane == 0) p.crc[u] = gf2_mul(r1, p.seg2_shift) ^ r2 ^ p.init_term;
   }
@@ -191,7 +204,8 @@ __global__ void __launch_bounds__(kThreads) k_crc32_split(const __grid_constant_
       const int64_t g0 = k * p.chunk_groups;
       const int64_t g1 = g0 + p.chunk_groups < groups ? g0 + p.chunk_groups : groups;
       const int64_t first = words - groups * 32 * kCrcGroup + lane;
-      r = lane_tree(maps, group_range(maps, reinterpret_cast<const uint4*>(a), first, g0, g1), lane);
+      r = lane_tree(maps, group_range(maps, reinterpret_cast<const uint4*>(a), first, lane, g0, g1),
+                    lane);
       if (lane == 0) {
         // x^(8 * 16 * 32 * kCrcGroup * (groups - g1)) from the host's powers of two
         uint32_t m = 0x80000000u;
@@ -201,7 +215,10 @@ __global__ void __launch_bounds__(kThreads) k_crc32_split(const __grid_constant_
       }
     } else {
       const uint8_t* b = p.b_bytes > 0 ? p.b + u * p.b_stride : nullptr;
-      r = t + p.b_bytes > 0 ? byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane) : 0u;
+      r = 0;
+      if (t + p.b_bytes > 0)
+        r = p.b_words ? aligned_segment(maps, reinterpret_cast<const uint4*>(b), p.b_bytes >> 4, lane)
+                      : byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane);
       r ^= p.init_term;
     }
     if (lane == 0) atomicXor(p.crc + u, r);
@@ -246,6 +263,8 @@ cudaError_t launch_crc32(const CrcParams& in, cudaStream_t s) {
   std::memcpy(p.img_level, img.level, sizeof img.level);
   const uint64_t n = static_cast<uint64_t>(p.a_bytes + p.b_bytes);
   p.seg2_shift = crc_x_pow_bytes(static_cast<uint64_t>((p.a_bytes & 15) + p.b_bytes));
+  p.b_words = (p.a_bytes & 15) == 0 && p.b_bytes > 0 && p.b_bytes % 16 == 0 &&
+              reinterpret_cast<uintptr_t>(p.b) % 16 == 0 && (p.n_units == 1 || p.b_stride % 16 == 0);
   p.init_term = gf2_mul(0xFFFFFFFFu, crc_x_pow_bytes(n)) ^ 0xFFFFFFFFu;
   const int64_t resident = static_cast<int64_t>(device_sm_count()) * kCrcCtasPerSm;
   const int64_t groups = (p.a_bytes / 16 + 32 * kCrcGroup - 1) / (32 * kCrcGroup);

@@ -341,25 +341,41 @@ __device__ __forceinline__ void process_stage(const FetchParams& p, const Where&
 }
 
 // kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
+// A unit is the kFetchWarps sub-slabs of one CTA, one per warp.
+#ifndef HC_FETCH_WARPS
+#define HC_FETCH_WARPS 8
+#endif
+constexpr int kFetchWarps = HC_FETCH_WARPS;
+
+__host__ __device__ __forceinline__ uint32_t fetch_units(const SlabGrid& g) {
+  return (g.total + kFetchWarps - 1) / kFetchWarps;
+}
+
+// The warp's sub-slab in unit c (inactive past the last unit; c may be up to
+// three grids past it, which the 32-bit product must not wrap into range).
+__device__ __forceinline__ Where unit_warp(const SlabGrid& g, uint32_t c, uint32_t units, int warp) {
+  return locate(g, c < units ? c * kFetchWarps + warp : g.total);
+}
+
 template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16, int kGroupLog2>
-__global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchParams p) {
+__global__ void __launch_bounds__(kFetchWarps * 32, HC_FETCH_MIN_BLOCKS) k_fetch(FetchParams p) {
   using St = Stage<W, OutT, D>;
   constexpr bool kDoubleBuffer = HC_FETCH_DOUBLE_BUFFER && W != kRaw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = lane % FetchGeom<D>::kLanesPerRow, r = lane / FetchGeom<D>::kLanesPerRow;
-  const uint32_t stride = gridDim.x;
+  const uint32_t stride = gridDim.x, units = fetch_units(p.grid);
   uint32_t c = blockIdx.x;
-  if (c >= p.grid.units) return;
-  Where w0 = locate(p.grid, c * kWarps + warp);
+  if (c >= units) return;
+  Where w0 = locate(p.grid, c * kFetchWarps + warp);
   Info i0 = fetch_info(p, w0);
   if constexpr (kDoubleBuffer) {
-    Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
+    Where w1 = unit_warp(p.grid, c + stride, units, warp);
     Info i1 = fetch_info(p, w1);
     St cur;
     load_codes<W, OutT, D, kHalfSplit, kScaleF16, kGroupLog2>(p, w0, q, r, cur);
     load_table<W, OutT, D, kHalfSplit>(p, w0, i0, q, cur);
-    for (; c < p.grid.units; c += stride) {
-      const Where w2 = locate(p.grid, (c + 2 * stride) * kWarps + warp);
+    for (; c < units; c += stride) {
+      const Where w2 = unit_warp(p.grid, c + 2 * stride, units, warp);
       const Info i2 = fetch_info(p, w2);
       St nxt;
       load_codes<W, OutT, D, kHalfSplit, kScaleF16, kGroupLog2>(p, w1, q, r, nxt);
@@ -378,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchPa
       load_table<W, OutT, D, kHalfSplit>(p, w0, i0, q, cur);
       process_stage<W, OutT, D, kHalfSplit, kScaleF16>(p, w0, i0, q, r, lane, cur);
       c += stride;
-      if (c >= p.grid.units) break;  // one unit per CTA: no next unit
-      w0 = locate(p.grid, c * kWarps + warp);
+      if (c >= units) break;  // one unit per CTA: no next unit
+      w0 = locate(p.grid, c * kFetchWarps + warp);
       i0 = fetch_info(p, w0);
     }
   }
@@ -389,23 +405,32 @@ __global__ void __launch_bounds__(kThreads, HC_FETCH_MIN_BLOCKS) k_fetch(FetchPa
 // The two share one set of block-table loads, and the V sub-slab (which is
 // not rotated) is decoded and stored while the K sub-slab's rotation-table row
 // is in flight, so the warp no longer idles on the chain block table ->
-// table row.  The two stages need about 80 registers: 3 CTAs per SM.
-// Measured on GB300 against the one-sub-slab-per-warp fetch at 4 CTAs/SM:
-// ragged INT4 per-layer calls B16 87.6% -> 90.7%, B64 90.1% -> 91.8% of the
-// copy peak; for the FP8 wire the same pairing measured 2 points slower on
-// the Llama-shaped fetch, so the FP8, row-scaled FP8 and RAW wires keep one
+// table row.  The two stages need about 88 registers.  Measured on GB300
+// against the one-sub-slab-per-warp fetch at 4 CTAs/SM: ragged INT4
+// per-layer calls B16 87.6% -> 90.7%, B64 90.1% -> 91.8% of the copy peak;
+// for the FP8 wire the same pairing measured 2 points slower on the
+// Llama-shaped fetch, so the FP8, row-scaled FP8 and RAW wires keep one
 // sub-slab per warp.
-constexpr int kPairMinBlocks = 3;
+// Warps are independent; CTAs of 4 warps, 5 per SM.  A CTA's slot is freed
+// only when its last warp ends, and 8-warp CTAs (3 per SM) lost about 3
+// points of the copy peak per ragged layer to that wait.
+#ifndef HC_FETCH_KV_WARPS
+#define HC_FETCH_KV_WARPS 4
+#endif
+#ifndef HC_FETCH_KV_MIN_BLOCKS
+#define HC_FETCH_KV_MIN_BLOCKS 5
+#endif
+constexpr int kPairWarps = HC_FETCH_KV_WARPS;
 
 template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16, int kGroupLog2>
-__global__ void __launch_bounds__(kThreads, kPairMinBlocks) k_fetch_kv(FetchParams p) {
+__global__ void __launch_bounds__(kPairWarps * 32, HC_FETCH_KV_MIN_BLOCKS) k_fetch_kv(FetchParams p) {
   using St = Stage<W, OutT, D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = lane % FetchGeom<D>::kLanesPerRow, r = lane / FetchGeom<D>::kLanesPerRow;
   // K sub-slab gk of the call; its flat index and its V partner's (the same
   // (layer, block) holds 2 H wps sub-slabs, K's first, then V's)
   const uint32_t half_total = p.grid.total / 2;
-  const uint32_t gk = blockIdx.x * kWarps + warp;
+  const uint32_t gk = blockIdx.x * kPairWarps + warp;
   uint32_t fk = p.grid.total, fv = p.grid.total;  // out of range: an inactive warp
   if (gk < half_total) {
     const uint32_t per_lj = p.grid.per_lj.d, half = per_lj / 2;
@@ -427,16 +452,16 @@ __global__ void __launch_bounds__(kThreads, kPairMinBlocks) k_fetch_kv(FetchPara
 template <typename OutT, int D, int W, bool kHalfSplit, bool kScaleF16>
 cudaError_t launch_t(const FetchParams& p, cudaStream_t s) {
   if constexpr (W == kInt4) {
-    const uint32_t grid = (p.grid.total / 2 + kWarps - 1) / kWarps;
+    const uint32_t grid = (p.grid.total / 2 + kPairWarps - 1) / kPairWarps;
     if (p.group_log2 == 5)
-      k_fetch_kv<OutT, D, W, kHalfSplit, kScaleF16, 5><<<grid, kThreads, 0, s>>>(p);
+      k_fetch_kv<OutT, D, W, kHalfSplit, kScaleF16, 5><<<grid, kPairWarps * 32, 0, s>>>(p);
     else
-      k_fetch_kv<OutT, D, W, kHalfSplit, kScaleF16, 0><<<grid, kThreads, 0, s>>>(p);
+      k_fetch_kv<OutT, D, W, kHalfSplit, kScaleF16, 0><<<grid, kPairWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
   } else {
     const uint32_t grid = static_cast<uint32_t>(std::min<int64_t>(
-        p.grid.units, static_cast<int64_t>(device_sm_count()) * HC_FETCH_CTAS_PER_SM));
-    k_fetch<OutT, D, W, kHalfSplit, kScaleF16, 0><<<grid, kThreads, 0, s>>>(p);
+        fetch_units(p.grid), static_cast<int64_t>(device_sm_count()) * HC_FETCH_CTAS_PER_SM));
+    k_fetch<OutT, D, W, kHalfSplit, kScaleF16, 0><<<grid, kFetchWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
   }
 }

@@ -134,6 +134,7 @@ struct CrcParams {
   uint32_t n_units;
   uint32_t* crc;
   uint32_t seg2_shift;  // x^(8 * bytes of the second segment)
+  int32_t b_words;      // the second segment is b alone, whole 16-byte words, 16-byte aligned
   uint32_t init_term;   // the initial register's term and the final xor
   // split launch (few, large units): chunks per unit, groups per chunk, and
   // x^(8 * bytes of 2^i groups)

@@ -28,9 +28,10 @@ def _u32(t):
 SHAPES = [(0, 0, 0, 0, 3), (0, 16, 5, 7, 4), (1, 16, 0, 0, 5), (15, 16, 3, 3, 2),
           (16, 32, 0, 0, 9), (4095, 4096, 1, 1, 3), (4096, 4096, 64, 64, 17),
           (4096 + 48, 4160, 13, 20, 6), (32768, 32768, 64, 64, 40), (65536 + 16, 65552, 0, 0, 3),
-          (131072, 131072, 2048, 2048, 2),
+          (131072, 131072, 2048, 2048, 2), (0, 0, 32, 48, 4), (4096, 4096, 4800, 4800, 5),
+          (4096, 4096, 4800, 4808, 3),
           # few, large units: each unit is cut into chunks across warps
-          (262144 + 3, 262160, 0, 0, 1), (1 << 20, 1 << 20, 0, 0, 5),
+          (262144 + 3, 262160, 0, 0, 1), (1 << 20, 1 << 20, 0, 0, 5), (4 << 20, 4 << 20, 4096, 4096, 2),
           (8 * 2 ** 20 + 4100, 8 * 2 ** 20 + 4112, 77, 80, 3), (64 * 2 ** 20 + 5, 64 * 2 ** 20 + 16, 13, 13, 1)]
 
 
@@ -45,6 +46,23 @@ def test_crc32_units(a_bytes, a_stride, b_bytes, b_stride, n):
     hc.hc_crc32(da, a_bytes, a_stride, db if b_bytes else None, b_bytes, b_stride, n, out)
     torch.cuda.synchronize()
     want = ocrc.crc32_units(a, a_bytes, a_stride, n, b if b_bytes else None, b_bytes, b_stride)
+    assert np.array_equal(_u32(out), want)
+
+
+@pytest.mark.parametrize("offset", [0, 4, 8, 16])
+def test_crc32_second_segment_alignment(offset):
+    """b as whole 16-byte words is read word by word when it starts on a
+    16-byte boundary, byte by byte otherwise; both give the oracle's CRC."""
+    from kv_cache_quantization_hc_gb300 import hc
+    r = np.random.default_rng(offset)
+    n, a_bytes, b_bytes = 7, 2048, 4096 + 64
+    a = r.integers(0, 256, a_bytes * n, dtype=np.uint8)
+    b = r.integers(0, 256, b_bytes * n + offset, dtype=np.uint8)
+    da, db = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    out = torch.zeros(n, dtype=torch.int32, device=DEV)
+    hc.hc_crc32(da, a_bytes, a_bytes, db[offset:], b_bytes, b_bytes, n, out)
+    torch.cuda.synchronize()
+    want = ocrc.crc32_units(a, a_bytes, a_bytes, n, b[offset:], b_bytes, b_bytes)
     assert np.array_equal(_u32(out), want)
 
 
