@@ -661,7 +661,9 @@ __global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerS
   const int chunk = lane % G::kChunksPerRow, rr = lane / G::kChunksPerRow;
   const uint32_t stride = gridDim.x;
   uint32_t c = blockIdx.x;
-  if (c >= p.grid.units) return;  // uniform over the CTA
+  // a flat launch's CTA is one unit of flat_warps(B) sub-slabs, whole slabs
+  const int unit_warps = kFlat ? static_cast<int>(blockDim.x >> 5) : kWarps;
+  if (!kFlat && c >= p.grid.units) return;  // uniform over the CTA
 
   auto process = [&](const Where& w, const SlotInfo& si, const Raw8<SrcT>(&raw)[G::kPasses],
                      int parity) {
@@ -673,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerS
   };
   constexpr bool kZeroPad = kWire == 0;
 
-  Where w0 = locate(p.grid, c * kWarps + warp);
+  Where w0 = locate(p.grid, c * unit_warps + warp);
   SlotInfo s0 = fetch_slot(p, w0);
   if constexpr (kFlat) {  // the grid has one CTA per unit
     Raw8<SrcT> cur[G::kPasses];
@@ -714,6 +716,25 @@ __global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerS
   }
 }
 
+// Flat launches: CTAs of HC_ENCODE_FLAT_WARPS warps, or of one slab's warps
+// where a slab is larger (a slab's warps combine through shared memory, so a
+// CTA holds whole slabs).  Like the INT4 encode's, smaller CTAs wait less
+// for their slowest warp before the slot is freed.
+#ifndef HC_ENCODE_FLAT_WARPS
+#define HC_ENCODE_FLAT_WARPS 4
+#endif
+inline int flat_warps(const EncodeParams& p) {
+  return std::max(HC_ENCODE_FLAT_WARPS, 1 << p.grid.wps_log2);
+}
+
+// The fused CRC keeps 8-warp CTAs: each CTA fills its CRC tables first.
+template <typename SrcT, int D, int kWire, int kGroupLog2, bool kCrc = false>
+void launch_flat(const EncodeParams& p, cudaStream_t s) {
+  const int w = kCrc ? kWarps : flat_warps(p);
+  const uint32_t ctas = (p.grid.total + w - 1) / w;
+  k_encode<SrcT, D, kWire, true, kGroupLog2, kCrc><<<ctas, 32 * w, 0, s>>>(p);
+}
+
 // Launch shape: 16-bit INT4, and 16-bit FP8 with blocks over 16 tokens, one
 // unit per CTA; everything else persistent (fp32 sources hold twice the
 // registers per row).
@@ -723,11 +744,11 @@ void encode_launch(const EncodeParams& p, cudaStream_t s) {
     const uint32_t ctas = (p.grid.total + kInt4EncodeWarps - 1) / kInt4EncodeWarps;
     k_encode_int4_wide<SrcT, D, kGroupLog2><<<ctas, kInt4EncodeWarps * 32, 0, s>>>(p);
   } else if constexpr (sizeof(SrcT) == 2 && kWire != 0) {
-    k_encode<SrcT, D, kWire, true, kGroupLog2><<<p.grid.units, kThreads, 0, s>>>(p);
+    launch_flat<SrcT, D, kWire, kGroupLog2>(p, s);
   } else {
     if constexpr (sizeof(SrcT) == 2) {
       if (p.B > kRowsPerWarp) {
-        k_encode<SrcT, D, kWire, true, kGroupLog2><<<p.grid.units, kThreads, 0, s>>>(p);
+        launch_flat<SrcT, D, kWire, kGroupLog2>(p, s);
         return;
       }
     }
@@ -795,7 +816,7 @@ void make_slab_crc_constants(int d, int block_size, EncodeParams* p) {
 template <typename SrcT, int D>
 cudaError_t encode_crc_t(const EncodeParams& p, cudaStream_t s) {
   if (p.B > kRowsPerWarp) {
-    k_encode<SrcT, D, 0, true, 0, true><<<p.grid.units, kThreads, 0, s>>>(p);
+    launch_flat<SrcT, D, 0, 0, true>(p, s);
   } else {
     const uint32_t grid = static_cast<uint32_t>(
         std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * kFusedCrcCtasPerSm));
