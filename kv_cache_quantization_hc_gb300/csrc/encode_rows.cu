@@ -33,8 +33,17 @@ __device__ __forceinline__ float div448(float a) {
   return a >= 0x1p-116f ? div7(a) * 0x1p-6f : __fdiv_rn(a, 448.0f);
 }
 
+// Warps are independent (one sub-slab each, a scale per row): CTAs of
+// kRowsWarps warps, 4 (8 per SM for 16-bit sources), which measured 0.75%
+// faster than 8-warp CTAs on the Qwen3-8B step.
+#ifndef HC_ROWS_ENCODE_WARPS
+#define HC_ROWS_ENCODE_WARPS 4
+#endif
+constexpr int kRowsWarps = HC_ROWS_ENCODE_WARPS;
+
 template <typename SrcT, int D, bool kScaleF16>
-__global__ void __launch_bounds__(kThreads, sizeof(SrcT) == 2 ? 4 : 2) k_encode_fp8_rows(EncodeParams p) {
+__global__ void __launch_bounds__(kRowsWarps * 32, (sizeof(SrcT) == 2 ? 4 : 2) * 8 / kRowsWarps)
+    k_encode_fp8_rows(EncodeParams p) {
   constexpr int kRaws = sizeof(SrcT) == 2 ? 2 : 1;  // Raw8 pieces (8 elements) per lane and row
   constexpr int kElems = 8 * kRaws;
   constexpr int kLanesPerRow = D / kElems;
@@ -42,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, sizeof(SrcT) == 2 ? 4 : 2) k_encode_
   constexpr int kPasses = kRowsPerWarp / kRowsPerPass;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = lane % kLanesPerRow, rr = lane / kLanesPerRow;
-  const Where w = locate(p.grid, blockIdx.x * kWarps + warp);
+  const Where w = locate(p.grid, blockIdx.x * kRowsWarps + warp);
   if (!w.active) return;
   const SlotInfo si = fetch_slot(p, w);
   const int bad = slot_errors(p, si);
@@ -103,10 +112,11 @@ __global__ void __launch_bounds__(kThreads, sizeof(SrcT) == 2 ? 4 : 2) k_encode_
 
 template <typename SrcT, int D>
 cudaError_t rows_t(bool scale_f16, const EncodeParams& p, cudaStream_t s) {
+  const uint32_t ctas = (p.grid.total + kRowsWarps - 1) / kRowsWarps;
   if (scale_f16)
-    k_encode_fp8_rows<SrcT, D, true><<<p.grid.units, kThreads, 0, s>>>(p);
+    k_encode_fp8_rows<SrcT, D, true><<<ctas, kRowsWarps * 32, 0, s>>>(p);
   else
-    k_encode_fp8_rows<SrcT, D, false><<<p.grid.units, kThreads, 0, s>>>(p);
+    k_encode_fp8_rows<SrcT, D, false><<<ctas, kRowsWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -16,14 +16,14 @@
 // interleaved pairs (low[2e], low[2e+1]) and (high[2e], high[2e+1]).  d/16
 // lanes cover a row, 512/d rows per pass.
 //
-// A CTA covers a unit of 8 consecutive sub-slabs; by default there is one
-// unit per CTA and 4 CTAs per SM (the register budget is sized for that), as
+// A CTA covers a unit of 4 consecutive sub-slabs; by default there is one
+// unit per CTA and 7 CTAs per SM (the register budget is sized for that), as
 // this write-heavy kernel gains more from resident warps than from software
 // pipelining.  The same code runs persistent CTAs that step through units
 // with a per-warp prefetch of the next unit when built with
 // HC_FETCH_CTAS_PER_SM / HC_FETCH_DOUBLE_BUFFER (see hc_internal.cuh).
 // Each store instruction writes 8 output elements per lane; neighbouring
-// lanes write neighbouring 16-byte pieces of one token row, and the 8 warps
+// lanes write neighbouring 16-byte pieces of one token row, and the warps
 // of a unit write neighbouring heads.  Stores are streaming (measured faster
 // than write-back stores here).  Products are formed two at a time
 // (FMUL2 / FFMA2).
@@ -343,7 +343,7 @@ __device__ __forceinline__ void process_stage(const FetchParams& p, const Where&
 // kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
 // A unit is the kFetchWarps sub-slabs of one CTA, one per warp.
 #ifndef HC_FETCH_WARPS
-#define HC_FETCH_WARPS 8
+#define HC_FETCH_WARPS 4
 #endif
 constexpr int kFetchWarps = HC_FETCH_WARPS;
 
