@@ -45,7 +45,12 @@ KERNEL_SOURCES = {
     "k_fetch": ["fetch_impl.cuh", "fetch_fp8.cu", "hc_internal.cuh", "fastdiv.h"],
     "k_encode_fp8_rows": ["encode_rows.cu", "encode_common.cuh", "hc_internal.cuh", "fastdiv.h"],
     "k_fetch_fp8_rows": ["fetch_impl.cuh", "fetch_fp8_rows.cu", "hc_internal.cuh", "fastdiv.h"],
+    "k_crc32": ["crc32.cu", "crc_fields.cuh", "crc_math.h", "hc_internal.cuh"],
 }
+# Integer ALU pipe of one SM: 4 schedulers x 16 lanes (ncu's pct_of_peak for
+# the pipe is taken against this rate); GB300's maximum SM clock.
+ALU_LANES_PER_SM = 64
+MAX_SM_MHZ = 2070.0
 CODECS = {
     "fp8": "FP8 E4M3 wire (per-block-head fp32 scale)",
     "fp8_rows": "FP8 E4M3 wire (per-token-head fp16 scale, the pages' frame layout)",
@@ -101,30 +106,42 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, workload):
-    """DRAM traffic of one launch recorded by ncu in profiles/ (a capture of
-    the full-size launch), if the kernel's sources are unchanged since; else
-    None.  Returns {"traffic", "read", "write", "capture"}."""
+def profiled_values(kernel, workload, keys):
+    """Per-launch counters recorded by ncu in profiles/<kernel>_<workload>.md
+    (lines `key: value`), if the kernel's sources are unchanged since the
+    capture; else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         with open(path) as f:
             text = f.read()
     except OSError:
         return None
-    keys = ("dram_read_bytes_per_launch", "dram_write_bytes_per_launch", "source_sha256", "capture")
+    want = tuple(keys) + ("source_sha256", "capture")
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(keys):
+        if ":" in line and line.strip().startswith(want):
             k, v = line.split(":", 1)
             vals[k.strip().strip("-* `")] = v.strip().strip("`")
     if vals.get("source_sha256") != kernel_source_hash(kernel):
         return None
     try:
-        rd, wr = int(vals["dram_read_bytes_per_launch"]), int(vals["dram_write_bytes_per_launch"])
+        out = {k: int(vals[k]) for k in keys}
     except (KeyError, ValueError):
         return None
-    return {"traffic": rd + wr, "read": rd, "write": wr, "capture": vals.get("capture"),
-            "source": f"profiles/{kernel}_{workload}.md"}
+    out["capture"] = vals.get("capture")
+    out["source"] = f"profiles/{kernel}_{workload}.md"
+    return out
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM traffic of one launch recorded by ncu in profiles/ (a capture of
+    the full-size launch), if the kernel's sources are unchanged since; else
+    None.  Returns {"traffic", "read", "write", "capture", "source"}."""
+    v = profiled_values(kernel, workload, ("dram_read_bytes_per_launch", "dram_write_bytes_per_launch"))
+    if v is None:
+        return None
+    rd, wr = v["dram_read_bytes_per_launch"], v["dram_write_bytes_per_launch"]
+    return {"traffic": rd + wr, "read": rd, "write": wr, "capture": v["capture"], "source": v["source"]}
 
 
 class ClockSampler:
@@ -364,6 +381,28 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def crc_alu_roofline(p, seconds, device):
+    """The CRC kernel against its bound, the integer ALU pipe: ALU-pipe
+    warp instructions of one full-size launch (ncu, recorded in profiles/)
+    over the live launch time, against SMs x 64 lanes x the maximum SM
+    clock.  None unless the recorded launch is this one (the Qwen3-8B FP8
+    wire, all layers) and the kernel is unchanged since."""
+    import torch
+    if p.L != 36 or p.wire_name != "fp8":
+        return None
+    v = profiled_values("k_crc32", "qwen3_8b", ("alu_warp_instructions_per_launch",))
+    if v is None:
+        return None
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    achieved = v["alu_warp_instructions_per_launch"] * 32 / seconds / 1e12
+    peak_t = sms * ALU_LANES_PER_SM * MAX_SM_MHZ * 1e6 / 1e12
+    return {"bound": "alu", "achieved": achieved, "peak": peak_t,
+            "unit": "T integer-ALU thread instructions/s", "frac": achieved / peak_t,
+            "alu_warp_instructions_per_launch": v["alu_warp_instructions_per_launch"],
+            "peak_rule": f"{sms} SMs x {ALU_LANES_PER_SM} ALU lanes x {MAX_SM_MHZ:.0f} MHz",
+            "source": v["source"]}
+
+
 def run_crc(args, p, device, src_k, src_v):
     """CRC-32 of the step's wire (one unit per (layer, block): its codes, then
     its scales), timed alone with CUDA events after the step's own timing.
@@ -387,7 +426,8 @@ def run_crc(args, p, device, src_k, src_v):
     out_d = {"kernel": "k_crc32", "units": p.L * p.nb, "bytes_per_launch": nbytes, "launches": reps,
              "avg_ms": avg * 1e3, "gbs": nbytes / avg / 1e9, "frac": nbytes / avg / 1e9 / peak,
              "bound": "integer ALU: field extraction for the 5-bit table lookups (the traffic is "
-                      "read-only HBM)"}
+                      "read-only HBM)",
+             "roofline": crc_alu_roofline(p, avg, device)}
     if args.codec == "fp8":
         slab_crc = torch.empty((p.L, p.nb, 2, p.H), dtype=torch.int32, device=device)
 
