@@ -381,19 +381,17 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def crc_alu_roofline(p, seconds, device):
+def crc_alu_roofline(p, seconds, sms):
     """The CRC kernel against its bound, the integer ALU pipe: ALU-pipe
     warp instructions of one full-size launch (ncu, recorded in profiles/)
     over the live launch time, against SMs x 64 lanes x the maximum SM
     clock.  None unless the recorded launch is this one (the Qwen3-8B FP8
     wire, all layers) and the kernel is unchanged since."""
-    import torch
     if p.L != 36 or p.wire_name != "fp8":
         return None
     v = profiled_values("k_crc32", "qwen3_8b", ("alu_warp_instructions_per_launch",))
     if v is None:
         return None
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
     achieved = v["alu_warp_instructions_per_launch"] * 32 / seconds / 1e12
     peak_t = sms * ALU_LANES_PER_SM * MAX_SM_MHZ * 1e6 / 1e12
     return {"bound": "alu", "achieved": achieved, "peak": peak_t,
@@ -427,7 +425,8 @@ def run_crc(args, p, device, src_k, src_v):
              "avg_ms": avg * 1e3, "gbs": nbytes / avg / 1e9, "frac": nbytes / avg / 1e9 / peak,
              "bound": "integer ALU: field extraction for the 5-bit table lookups (the traffic is "
                       "read-only HBM)",
-             "roofline": crc_alu_roofline(p, avg, device)}
+             "roofline": crc_alu_roofline(
+                 p, avg, torch.cuda.get_device_properties(device).multi_processor_count)}
     if args.codec == "fp8":
         slab_crc = torch.empty((p.L, p.nb, 2, p.H), dtype=torch.int32, device=device)
 

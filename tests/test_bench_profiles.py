@@ -39,3 +39,18 @@ def test_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("k_fetch") == h0
     _sources(tmp_path, "k_fetch", "int f(int x) { return x + 2; }\n")
     assert bench.kernel_source_hash("k_fetch") != h0
+
+
+def test_crc_alu_roofline(monkeypatch):
+    """The CRC's roofline against the integer ALU: recorded ALU-pipe warp
+    instructions x 32 over the live time, against SMs x 64 lanes x 2070 MHz;
+    only for the launch the count was recorded on."""
+    from types import SimpleNamespace
+    monkeypatch.setattr(bench, "profiled_values", lambda k, w, keys: {
+        "alu_warp_instructions_per_launch": 350_000_000, "capture": "c", "source": "s"})
+    r = bench.crc_alu_roofline(SimpleNamespace(L=36, wire_name="fp8"), 0.7e-3, 152)
+    assert r["bound"] == "alu" and abs(r["peak"] - 152 * 64 * 2.07e9 / 1e12) < 1e-9
+    assert abs(r["achieved"] - 350e6 * 32 / 0.7e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+    assert bench.crc_alu_roofline(SimpleNamespace(L=4, wire_name="fp8"), 0.7e-3, 152) is None
+    assert bench.crc_alu_roofline(SimpleNamespace(L=36, wire_name="int4"), 0.7e-3, 152) is None

@@ -62,3 +62,20 @@ def test_per_layer_workload_objects():
     w.L = 2
     r = bench.measure_layered(w, "int4", dev, steps=3, warmup=3)
     assert set(r["fetch"]) == {"B16", "B64"} and r["tokens"] == sum(b.tokens() for b in w.blocks)
+
+
+def test_crc_leg_object():
+    """`--crc` adds the CRC-32 of the step's wire and the fused slab CRC; its
+    integer-ALU roofline is given only for the full launch whose ALU count
+    profiles/ records, so on a 2-layer cut it is null."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--layers", "2",
+                        "--steps", "3", "--warmup", "3", "--legs", "device", "--crc"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip().startswith("{")][-1])
+    c = d["crc32"]
+    assert c["kernel"] == "k_crc32" and c["units"] == 2 * 2048 and c["gbs"] > 0
+    assert c["bytes_per_launch"] == 2 * 2048 * (32768 + 64)
+    assert c["roofline"] is None
+    f = c["fused_encode"]
+    assert f["encode_with_crc_ms"] > 0 and f["encode_ms"] > 0
