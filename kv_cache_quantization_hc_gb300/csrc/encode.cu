@@ -279,32 +279,66 @@ __device__ __forceinline__ void load_rows(const EncodeParams& p, const Where& w,
 // warp reads without bank collisions.  A lane's code pieces (8 bytes per
 // pass) lie 256 bytes apart; the map of pass i takes a piece straight to its
 // contribution at the end of the lane's last piece, so a pass costs 13
-// lookups.  After the last pass a butterfly over the lanes (crc_lane_tree)
-// brings the warp's register to the end of the sub-slab, the sub-slabs of a
-// slab combine in shared memory (crc_sub), and the register is moved past the
-// scale's 4 bytes, which are added with the initial register's term and the
-// final xor.  The images of the maps' single-bit inputs come from the host
-// (make_slab_crc_constants); each CTA fills its tables once.
-template <int kPasses>
+// lookups.  After the last pass the lanes' registers are brought to the end
+// of the sub-slab and added: in persistent CTAs each lane moves its own
+// register there with a map of its own (kLaneShift, 7 lookups, tables laid
+// out so that every lane reads only its own bank) and shuffles add them; in
+// flat CTAs, which fill their tables per unit, a butterfly over the lanes
+// (crc_lane_tree, 35 lookups) does it with shared tables.  The sub-slabs of a
+// slab combine in shared memory (crc_sub), and the register is moved past
+// the scale's 4 bytes, which are added with the initial register's term and
+// the final xor.  The images of the maps' single-bit inputs come from the
+// host (make_slab_crc_constants); each CTA fills its tables once.
+template <int kPasses, bool kLaneShift>
 struct SlabCrcMaps {
   FieldMap<64> pos[kPasses];  // pass i's 8 code bytes -> the lane's register at its last piece
   FieldMap<32> level[5];      // a register -> the register 8 * 2^j bytes later
   FieldMap<32> tail;          // a register -> the register after the 4 scale bytes
   FieldMap<32> scale;         // the scale's 4 bytes -> the register after them
+  // lane l's register -> the register 8 (31 - l) bytes later, at the end of
+  // the sub-slab: entry [f][e][l] for field f of value e, so lane l reads
+  // bank l only
+  uint32_t lane_shift[kLaneShift ? 7 : 1][kLaneShift ? 32 : 1][kLaneShift ? 32 : 1];
 };
 
-template <int kPasses>
-__device__ __forceinline__ void build_slab_crc_maps(const EncodeParams& p, SlabCrcMaps<kPasses>& m) {
+template <int kPasses, bool kLaneShift>
+__device__ __forceinline__ void build_slab_crc_maps(const EncodeParams& p,
+                                                    SlabCrcMaps<kPasses, kLaneShift>& m) {
   for (int i = 0; i < kPasses; ++i) fill_field_map<64>(m.pos[i], p.crc_img_pos[i]);
   for (int j = 0; j < 5; ++j) fill_field_map<32>(m.level[j], p.crc_img_level[j]);
   fill_field_map<32>(m.tail, p.crc_img_tail);
   fill_field_map<32>(m.scale, p.crc_img_scale);
   __syncthreads();
+  if constexpr (kLaneShift) {
+    // the shift by 8 (31 - l) bytes is the product of the level maps of the
+    // set bits of 31 - l
+    for (int i = threadIdx.x; i < 7 * 32 * 32; i += blockDim.x) {
+      const int f = i >> 10, e = (i >> 5) & 31, l = i & 31;
+      uint32_t v = static_cast<uint32_t>(e) << (5 * f);
+#pragma unroll
+      for (int j = 0; j < 5; ++j)
+        if (((31 - l) >> j) & 1) v = apply_map(m.level[j], v);
+      m.lane_shift[f][e][l] = v;
+    }
+    __syncthreads();
+  }
 }
 
 __device__ __forceinline__ uint32_t crc_piece(const FieldMap<64>& m, uint2 c) {
   const uint32_t v[2] = {c.x, c.y};
   return apply_map<64>(m, v);
+}
+
+// The warp's register, in every lane, from each lane's (positioned at the
+// end of the lane's last piece, 8 (31 - l) bytes before the sub-slab's end).
+__device__ __forceinline__ uint32_t crc_lane_shift(const uint32_t (&t)[7][32][32], uint32_t acc,
+                                                   int lane) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int f = 0; f < 7; ++f) r ^= t[f][(acc >> (5 * f)) & 31u][lane];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) r ^= __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
 }
 
 // The warp's register from each lane's (positioned at the end of the lane's
@@ -323,11 +357,11 @@ __device__ __forceinline__ uint32_t crc_lane_tree(const FieldMap<32> (&level)[5]
   return acc;
 }
 
-template <typename SrcT, int D, bool kCrc>
+template <typename SrcT, int D, bool kCrc, typename Maps>
 __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where& w,
                                              const SlotInfo& si, int chunk, int rr, int warp,
                                              int lane, float* s_amax, uint32_t* s_crc,
-                                             const SlabCrcMaps<EncodeGeom<D>::kPasses>* maps,
+                                             const Maps* maps,
                                              const Raw8<SrcT> (&raw)[EncodeGeom<D>::kPasses]) {
   using G = EncodeGeom<D>;
   const int bad = w.active ? slot_errors(p, si) : 0;
@@ -382,7 +416,10 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
     }
     if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
     if constexpr (kCrc) {
-      acc = crc_lane_tree(maps->level, acc, lane);  // lane 0: the sub-slab's register
+      if constexpr (sizeof(maps->lane_shift) > 4)
+        acc = crc_lane_shift(maps->lane_shift, acc, lane);  // every lane: the sub-slab's register
+      else
+        acc = crc_lane_tree(maps->level, acc, lane);  // lane 0: the sub-slab's register
       if (wps > 1) {
         if (lane == 0) s_crc[warp] = acc;
         __syncthreads();
@@ -650,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerS
   static_assert(!kCrc || (kWire == 0 && sizeof(SrcT) == 2), "fused CRC: FP8, 16-bit sources");
   __shared__ float s_amax[2][kWarps];
   __shared__ uint32_t s_crc[2][kWarps];
-  using Maps = SlabCrcMaps<G::kPasses>;
+  using Maps = SlabCrcMaps<G::kPasses, !kFlat>;
   __shared__ typename std::conditional<kCrc, Maps, char>::type crc_maps;
   const Maps* maps = nullptr;
   if constexpr (kCrc) {
