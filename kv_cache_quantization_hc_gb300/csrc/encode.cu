@@ -11,10 +11,11 @@
 // Work decomposition.  One warp owns a 16-token sub-slab of one (layer,
 // block, kv, head); each lane owns one 8-element chunk of a token row
 // (16 bytes for fp16/bf16, 32 for fp32) per pass, 256/d rows per pass, d/16
-// passes.  A CTA's 8 warps take a "unit" of 8 consecutive sub-slabs.  Two
-// launch shapes, chosen by measurement on GB300: one unit per CTA at 4 CTAs
-// per SM (16-bit INT4, and 16-bit FP8 with blocks over 16 tokens), or
-// persistent CTAs, two per SM, stepping through the units with a three-deep
+// passes.  A CTA's warps take a "unit" of as many consecutive sub-slabs.
+// Two launch shapes, chosen by measurement on GB300: one unit per CTA (16-bit
+// INT4 in 4-warp CTAs; 16-bit FP8 with blocks over 16 tokens in CTAs of one
+// slab's warps, at least 4), or persistent 8-warp CTAs, two per SM, stepping
+// through the units with a three-deep
 // pipeline per warp: the block table entry for unit i+2 is requested, the
 // rows of unit i+1 are loaded (16-bit sources: into a second register
 // buffer), and unit i is quantized and stored - so neither the table lookup
@@ -672,8 +673,9 @@ __global__ void __launch_bounds__(kInt4EncodeWarps * 32, HC_ENCODE_WIDE_MIN_BLOC
 }
 
 // kWire: 0 = FP8, 1 = INT4 fp16 scales, 2 = INT4 fp32 scales.
-// kFlat: one unit per CTA at 4 CTAs per SM; otherwise persistent CTAs (2 per
-// SM) with the per-warp double buffer for 16-bit sources.  Measured on GB300,
+// kFlat: one unit per CTA (launch_flat: CTAs of whole slabs, at least 4
+// warps; 64 registers); otherwise persistent CTAs (2 per SM) with the
+// per-warp double buffer for 16-bit sources.  Measured on GB300,
 // the persistent pipeline is faster for FP8 with 16-token blocks, the flat
 // launch for FP8 with larger blocks (whose units meet at a CTA barrier) and
 // for INT4.

@@ -47,7 +47,7 @@ struct SlabGrid {
   FastDivmod heads;   // H
   uint32_t wps_log2;  // log2(block_size / 16)
   uint32_t total;     // sub-slabs in the call
-  uint32_t units;     // ceil(total / 8): one unit = the 8 warps of a CTA
+  uint32_t units;     // ceil(total / 8): units of the persistent 8-warp CTAs
 };
 
 struct EncodeParams {
@@ -99,15 +99,15 @@ struct TableParams {
 };
 
 // CRC-32 of units a[u*a_stride ..+a_bytes) ++ b[u*b_stride ..+b_bytes), one
-// warp per unit.  Lane k < 31 takes bytes [k*chunk, (k+1)*chunk) of the a
-// part, lane 31 the rest of it and the b part; each lane's register is moved
-// to the end of the unit by multiplying with lane_shift[k] = x^(8 * bytes
-// after its part) mod P, and init_term adds the initial register's
-// contribution and the final xor.  Constants are built on the host.
-// CRC-32 of units (crc32.cu): rows of 32 16-byte words are taken kCrcGroup
-// at a time, by persistent CTAs, kCrcCtasPerSm per SM.  Measured on GB300 over
+// warp per unit (crc32.cu): the unit's rows of 32 16-byte words, lane l
+// taking word l of each row, kCrcGroup rows at a time, by persistent CTAs,
+// kCrcCtasPerSm per SM; a butterfly over the lanes joins their registers,
+// seg2_shift moves the 16-byte-word segment's register past the second
+// segment, and init_term adds the initial register's contribution and the
+// final xor.  Constants are built on the host.  Measured on GB300 over
 // the Qwen3-8B-shaped FP8 wire (73,728 units of 32 KiB): groups of 4 rows at
-// 8 CTAs/SM 3.43 TB/s; at 4 CTAs/SM 3.17; groups of 8 rows 2.2-2.4.
+// 8 CTAs/SM 3.43 TB/s (3.68 with the multiply-high field extraction and the
+// scales read as words); at 4 CTAs/SM 3.17; groups of 8 rows 2.2-2.4.
 #ifndef HC_CRC_GROUP
 #define HC_CRC_GROUP 4
 #endif
@@ -121,8 +121,9 @@ constexpr int kCrcCtasPerSm = HC_CRC_CTAS_PER_SM;
 constexpr int kCrcMinChunkGroups = 64;
 // The encoder's fused slab CRC with 16-token blocks: persistent CTAs, 2 per
 // SM with the per-warp double buffer (128 registers), or 3-4 per SM with a
-// single buffer (64 registers).  Measured on the Qwen3-8B-shaped encode:
-// 1.66 ms (2), 1.67 ms (3), 1.63 ms (4); the plain encode takes 1.08 ms.
+// single buffer (64 registers).  Measured on the Qwen3-8B-shaped encode
+// (with the lane butterfly): 1.66 ms (2), 1.67 ms (3), 1.63 ms (4); the
+// plain encode takes 1.08 ms.
 #ifndef HC_FUSED_CRC_CTAS_PER_SM
 #define HC_FUSED_CRC_CTAS_PER_SM 4
 #endif
