@@ -311,14 +311,26 @@ __device__ __forceinline__ void build_slab_crc_maps(const EncodeParams& p,
   fill_field_map<32>(m.scale, p.crc_img_scale);
   __syncthreads();
   if constexpr (kLaneShift) {
-    // the shift by 8 (31 - l) bytes is the product of the level maps of the
-    // set bits of 31 - l
-    for (int i = threadIdx.x; i < 7 * 32 * 32; i += blockDim.x) {
-      const int f = i >> 10, e = (i >> 5) & 31, l = i & 31;
-      uint32_t v = static_cast<uint32_t>(e) << (5 * f);
+    // The shift by 8 (31 - l) bytes is the product of the level maps of the
+    // set bits of 31 - l.  First the images of single input bits (entries
+    // 1 << b; bits past 31 give 0), then every other entry as the xor of the
+    // entries of its bits.
+    for (int i = threadIdx.x; i < 7 * 5 * 32; i += blockDim.x) {
+      const int f = i / 160, b = (i >> 5) % 5, l = i & 31, q = 5 * f + b;
+      uint32_t v = q < 32 ? 1u << q : 0u;
 #pragma unroll
       for (int j = 0; j < 5; ++j)
         if (((31 - l) >> j) & 1) v = apply_map(m.level[j], v);
+      m.lane_shift[f][1 << b][l] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 7 * 32 * 32; i += blockDim.x) {
+      const int f = i >> 10, e = (i >> 5) & 31, l = i & 31;
+      if (e != 0 && (e & (e - 1)) == 0) continue;  // a single bit: set above
+      uint32_t v = 0;
+#pragma unroll
+      for (int b = 0; b < 5; ++b)
+        if ((e >> b) & 1) v ^= m.lane_shift[f][1 << b][l];
       m.lane_shift[f][e][l] = v;
     }
     __syncthreads();
