@@ -386,11 +386,11 @@ def crc_alu_roofline(p, seconds, sms):
     warp instructions of one full-size launch (ncu, recorded in profiles/)
     over the live launch time, against SMs x 64 lanes x the maximum SM
     clock.  None unless the recorded launch is this one (the Qwen3-8B FP8
-    wire, all layers) and the kernel is unchanged since."""
-    if p.L != 36 or p.wire_name != "fp8":
+    wire, as many units) and the kernel is unchanged since."""
+    if p.wire_name != "fp8":
         return None
-    v = profiled_values("k_crc32", "qwen3_8b", ("alu_warp_instructions_per_launch",))
-    if v is None:
+    v = profiled_values("k_crc32", "qwen3_8b", ("alu_warp_instructions_per_launch", "units_per_launch"))
+    if v is None or v["units_per_launch"] != p.L * p.nb:
         return None
     achieved = v["alu_warp_instructions_per_launch"] * 32 / seconds / 1e12
     peak_t = sms * ALU_LANES_PER_SM * MAX_SM_MHZ * 1e6 / 1e12

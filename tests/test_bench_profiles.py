@@ -47,10 +47,11 @@ def test_crc_alu_roofline(monkeypatch):
     only for the launch the count was recorded on."""
     from types import SimpleNamespace
     monkeypatch.setattr(bench, "profiled_values", lambda k, w, keys: {
-        "alu_warp_instructions_per_launch": 350_000_000, "capture": "c", "source": "s"})
-    r = bench.crc_alu_roofline(SimpleNamespace(L=36, wire_name="fp8"), 0.7e-3, 152)
+        "alu_warp_instructions_per_launch": 350_000_000, "units_per_launch": 36 * 2048,
+        "capture": "c", "source": "s"})
+    r = bench.crc_alu_roofline(SimpleNamespace(L=36, nb=2048, wire_name="fp8"), 0.7e-3, 152)
     assert r["bound"] == "alu" and abs(r["peak"] - 152 * 64 * 2.07e9 / 1e12) < 1e-9
     assert abs(r["achieved"] - 350e6 * 32 / 0.7e-3 / 1e12) < 1e-9
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
-    assert bench.crc_alu_roofline(SimpleNamespace(L=4, wire_name="fp8"), 0.7e-3, 152) is None
-    assert bench.crc_alu_roofline(SimpleNamespace(L=36, wire_name="int4"), 0.7e-3, 152) is None
+    assert bench.crc_alu_roofline(SimpleNamespace(L=4, nb=2048, wire_name="fp8"), 0.7e-3, 152) is None
+    assert bench.crc_alu_roofline(SimpleNamespace(L=36, nb=2048, wire_name="int4"), 0.7e-3, 152) is None
