@@ -280,25 +280,29 @@ __device__ __forceinline__ void load_rows(const EncodeParams& p, const Where& w,
 // warp reads without bank collisions.  A lane's code pieces (8 bytes per
 // pass) lie 256 bytes apart; the map of pass i takes a piece straight to its
 // contribution at the end of the lane's last piece, so a pass costs 13
-// lookups.  After the last pass the lanes' registers are brought to the end
-// of the sub-slab and added: in persistent CTAs each lane moves its own
-// register there with a map of its own (kLaneShift, 7 lookups, tables laid
-// out so that every lane reads only its own bank) and shuffles add them; in
-// flat CTAs, which fill their tables per unit, a butterfly over the lanes
-// (crc_lane_tree, 35 lookups) does it with shared tables.  The sub-slabs of a
-// slab combine in shared memory (crc_sub), and the register is moved past
-// the scale's 4 bytes, which are added with the initial register's term and
-// the final xor.  The images of the maps' single-bit inputs come from the
-// host (make_slab_crc_constants); each CTA fills its tables once.
+// lookups.  After the last pass the lanes' registers are combined.
+// Persistent CTAs run 16-token blocks, whose slab is one sub-slab: each lane
+// moves its own register past the rest of the slab and the scale's 4 bytes
+// with a map of its own (kLaneShift, 7 lookups, tables laid out so that
+// every lane reads only its own bank), lanes 0-6 add one field each of the
+// scale's contribution, and shuffles add it all.  Flat CTAs, which fill
+// their tables per unit, bring the registers to the end of the sub-slab with
+// a butterfly over the lanes (crc_lane_tree, 35 lookups) on shared tables;
+// the sub-slabs of a slab combine in shared memory (crc_sub), and the
+// register is moved past the scale's 4 bytes, which are added.  Last come
+// the initial register's term and the final xor.  The images of the maps'
+// single-bit inputs come from the host (make_slab_crc_constants); each CTA
+// fills its tables once.
 template <int kPasses, bool kLaneShift>
 struct SlabCrcMaps {
   FieldMap<64> pos[kPasses];  // pass i's 8 code bytes -> the lane's register at its last piece
   FieldMap<32> level[5];      // a register -> the register 8 * 2^j bytes later
   FieldMap<32> tail;          // a register -> the register after the 4 scale bytes
   FieldMap<32> scale;         // the scale's 4 bytes -> the register after them
-  // lane l's register -> the register 8 (31 - l) bytes later, at the end of
-  // the sub-slab: entry [f][e][l] for field f of value e, so lane l reads
-  // bank l only
+  // lane l's register -> the register 8 (31 - l) + 4 bytes later, after the
+  // slab's last code byte and its scale (persistent CTAs run 16-token
+  // blocks, whose slab is one sub-slab): entry [f][e][l] for field f of
+  // value e, so lane l reads bank l only
   uint32_t lane_shift[kLaneShift ? 7 : 1][kLaneShift ? 32 : 1][kLaneShift ? 32 : 1];
 };
 
@@ -312,16 +316,16 @@ __device__ __forceinline__ void build_slab_crc_maps(const EncodeParams& p,
   __syncthreads();
   if constexpr (kLaneShift) {
     // The shift by 8 (31 - l) bytes is the product of the level maps of the
-    // set bits of 31 - l.  First the images of single input bits (entries
-    // 1 << b; bits past 31 give 0), then every other entry as the xor of the
-    // entries of its bits.
+    // set bits of 31 - l, and the tail map adds the scale's 4.  First the
+    // images of single input bits (entries 1 << b; bits past 31 give 0),
+    // then every other entry as the xor of the entries of its bits.
     for (int i = threadIdx.x; i < 7 * 5 * 32; i += blockDim.x) {
       const int f = i / 160, b = (i >> 5) % 5, l = i & 31, q = 5 * f + b;
       uint32_t v = q < 32 ? 1u << q : 0u;
 #pragma unroll
       for (int j = 0; j < 5; ++j)
         if (((31 - l) >> j) & 1) v = apply_map(m.level[j], v);
-      m.lane_shift[f][1 << b][l] = v;
+      m.lane_shift[f][1 << b][l] = apply_map(m.tail, v);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 7 * 32 * 32; i += blockDim.x) {
@@ -342,11 +346,11 @@ __device__ __forceinline__ uint32_t crc_piece(const FieldMap<64>& m, uint2 c) {
   return apply_map<64>(m, v);
 }
 
-// The warp's register, in every lane, from each lane's (positioned at the
-// end of the lane's last piece, 8 (31 - l) bytes before the sub-slab's end).
+// The sum over the lanes of each lane's register moved past the lane's rest
+// of the slab (the lane maps) plus `add`, in every lane.
 __device__ __forceinline__ uint32_t crc_lane_shift(const uint32_t (&t)[7][32][32], uint32_t acc,
-                                                   int lane) {
-  uint32_t r = 0;
+                                                   uint32_t add, int lane) {
+  uint32_t r = add;
 #pragma unroll
   for (int f = 0; f < 7; ++f) r ^= t[f][(acc >> (5 * f)) & 31u][lane];
 #pragma unroll
@@ -428,11 +432,16 @@ __device__ __forceinline__ void quantize_fp8(const EncodeParams& p, const Where&
       }
     }
     if (w.sub == 0 && lane == 0) static_cast<float*>(p.scales)[w.slab] = s;
-    if constexpr (kCrc) {
-      if constexpr (sizeof(maps->lane_shift) > 4)
-        acc = crc_lane_shift(maps->lane_shift, acc, lane);  // every lane: the sub-slab's register
-      else
-        acc = crc_lane_tree(maps->level, acc, lane);  // lane 0: the sub-slab's register
+    if constexpr (kCrc && sizeof(maps->lane_shift) > 4) {
+      // Persistent CTAs run 16-token blocks only, so the sub-slab is the
+      // slab: each lane's map moves its register past the scale's 4 bytes
+      // too, lanes 0-6 add the scale's fields, and the shuffles add it all.
+      const uint32_t sb = __float_as_uint(s);  // the scale's 4 bytes, little-endian
+      const uint32_t scale_part = lane < 7 ? maps->scale.f[lane][(sb >> (5 * lane)) & 31u] : 0u;
+      acc = crc_lane_shift(maps->lane_shift, acc, scale_part, lane);
+      if (lane == 0) p.crc[w.slab] = acc ^ p.crc_init;
+    } else if constexpr (kCrc) {
+      acc = crc_lane_tree(maps->level, acc, lane);  // lane 0: the sub-slab's register
       if (wps > 1) {
         if (lane == 0) s_crc[warp] = acc;
         __syncthreads();
@@ -866,7 +875,8 @@ void make_slab_crc_constants(int d, int block_size, EncodeParams* p) {
 
 template <typename SrcT, int D>
 cudaError_t encode_crc_t(const EncodeParams& p, cudaStream_t s) {
-  if (p.B > kRowsPerWarp) {
+  // the persistent kernel's lane maps assume one sub-slab per slab
+  if (p.B != kRowsPerWarp) {
     launch_flat<SrcT, D, 0, 0, true>(p, s);
   } else {
     const uint32_t grid = static_cast<uint32_t>(
