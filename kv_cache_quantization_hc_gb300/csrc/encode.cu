@@ -703,13 +703,15 @@ __global__ void __launch_bounds__(kInt4EncodeWarps * 32, HC_ENCODE_WIDE_MIN_BLOC
 // kGroupLog2: INT4 group size fixed at compile time (5: g = 32), or 0.
 // kCrc: the FP8 wire with the fused slab CRC (16-bit sources).
 template <typename SrcT, int D, int kWire, bool kFlat, int kGroupLog2, bool kCrc = false>
-__global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerSm > 2)) ? 4 : 2)
+__global__ void __launch_bounds__((kCrc && !kFlat) ? kFusedCrcWarps * 32 : kThreads,
+                                  kFlat ? 4 : (kCrc ? kFusedCrcCtasPerSm : 2))
     k_encode(const __grid_constant__ EncodeParams p) {
   using G = EncodeGeom<D>;
   constexpr bool kDoubleBuffer = !kFlat && sizeof(SrcT) == 2 && !(kCrc && kFusedCrcCtasPerSm > 2);
   static_assert(!kCrc || (kWire == 0 && sizeof(SrcT) == 2), "fused CRC: FP8, 16-bit sources");
-  __shared__ float s_amax[2][kWarps];
-  __shared__ uint32_t s_crc[2][kWarps];
+  constexpr int kMaxWarps = (kCrc && !kFlat) ? kFusedCrcWarps : kWarps;
+  __shared__ float s_amax[2][kMaxWarps];
+  __shared__ uint32_t s_crc[2][kMaxWarps];
   using Maps = SlabCrcMaps<G::kPasses, !kFlat>;
   __shared__ typename std::conditional<kCrc, Maps, char>::type crc_maps;
   const Maps* maps = nullptr;
@@ -721,9 +723,11 @@ __global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerS
   const int chunk = lane % G::kChunksPerRow, rr = lane / G::kChunksPerRow;
   const uint32_t stride = gridDim.x;
   uint32_t c = blockIdx.x;
-  // a flat launch's CTA is one unit of flat_warps(B) sub-slabs, whole slabs
-  const int unit_warps = kFlat ? static_cast<int>(blockDim.x >> 5) : kWarps;
-  if (!kFlat && c >= p.grid.units) return;  // uniform over the CTA
+  // a CTA's unit is as many sub-slabs as it has warps (flat launches:
+  // flat_warps(B), whole slabs); persistent CTAs step through the units
+  const int unit_warps = static_cast<int>(blockDim.x >> 5);
+  const uint32_t units = kFlat ? gridDim.x : (p.grid.total + unit_warps - 1) / unit_warps;
+  if (!kFlat && c >= units) return;  // uniform over the CTA
 
   auto process = [&](const Where& w, const SlotInfo& si, const Raw8<SrcT>(&raw)[G::kPasses],
                      int parity) {
@@ -742,13 +746,13 @@ __global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerS
     load_rows<SrcT, D, kZeroPad>(p, w0, s0, chunk, rr, cur);
     process(w0, s0, cur, 0);
   } else if constexpr (kDoubleBuffer) {
-    Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
+    Where w1 = locate(p.grid, (c + stride) * unit_warps + warp);
     SlotInfo s1 = fetch_slot(p, w1);
     Raw8<SrcT> cur[G::kPasses];
     load_rows<SrcT, D, kZeroPad>(p, w0, s0, chunk, rr, cur);
     int parity = 0;
-    for (; c < p.grid.units; c += stride) {
-      const Where w2 = locate(p.grid, (c + 2 * stride) * kWarps + warp);
+    for (; c < units; c += stride) {
+      const Where w2 = locate(p.grid, (c + 2 * stride) * unit_warps + warp);
       const SlotInfo s2 = fetch_slot(p, w2);
       Raw8<SrcT> nxt[G::kPasses];
       load_rows<SrcT, D, kZeroPad>(p, w1, s1, chunk, rr, nxt);
@@ -763,8 +767,8 @@ __global__ void __launch_bounds__(kThreads, (kFlat || (kCrc && kFusedCrcCtasPerS
     }
   } else {
     int parity = 0;
-    for (; c < p.grid.units; c += stride) {
-      const Where w1 = locate(p.grid, (c + stride) * kWarps + warp);
+    for (; c < units; c += stride) {
+      const Where w1 = locate(p.grid, (c + stride) * unit_warps + warp);
       const SlotInfo s1 = fetch_slot(p, w1);
       Raw8<SrcT> cur[G::kPasses];
       load_rows<SrcT, D, kZeroPad>(p, w0, s0, chunk, rr, cur);
@@ -879,9 +883,10 @@ cudaError_t encode_crc_t(const EncodeParams& p, cudaStream_t s) {
   if (p.B != kRowsPerWarp) {
     launch_flat<SrcT, D, 0, 0, true>(p, s);
   } else {
+    const int64_t units = (static_cast<int64_t>(p.grid.total) + kFusedCrcWarps - 1) / kFusedCrcWarps;
     const uint32_t grid = static_cast<uint32_t>(
-        std::min<int64_t>(p.grid.units, static_cast<int64_t>(device_sm_count()) * kFusedCrcCtasPerSm));
-    k_encode<SrcT, D, 0, false, 0, true><<<grid, kThreads, 0, s>>>(p);
+        std::min<int64_t>(units, static_cast<int64_t>(device_sm_count()) * kFusedCrcCtasPerSm));
+    k_encode<SrcT, D, 0, false, 0, true><<<grid, kFusedCrcWarps * 32, 0, s>>>(p);
   }
   return cudaGetLastError();
 }

@@ -127,7 +127,11 @@ constexpr int kCrcMinChunkGroups = 64;
 #ifndef HC_FUSED_CRC_CTAS_PER_SM
 #define HC_FUSED_CRC_CTAS_PER_SM 4
 #endif
+#ifndef HC_FUSED_CRC_WARPS
+#define HC_FUSED_CRC_WARPS 8
+#endif
 constexpr int kFusedCrcCtasPerSm = HC_FUSED_CRC_CTAS_PER_SM;
+constexpr int kFusedCrcWarps = HC_FUSED_CRC_WARPS;  // warps per persistent CTA (16 at most)
 
 struct CrcParams {
   const uint8_t* a;
