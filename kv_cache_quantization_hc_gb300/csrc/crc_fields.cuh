@@ -57,7 +57,9 @@ __device__ __forceinline__ void fill_field_map(FieldMap<N>& m, const uint32_t* i
 // different shift instruction; both CRC kernels measured 2-3% faster with
 // it, and ncu still shows the FMA pipe idle and the ALU pipe busy, so the
 // bound is unchanged.  (The shift as a multiply-high of the unmasked word,
-// masked afterwards, measured 8-10% slower.)
+// masked afterwards, measured 8-10% slower; a multiplier of 2^(34 - s) + 1,
+// which gives the same high word but cannot become a shift, keeps a true
+// multiply-high on the FMA pipe and measured 19% slower.)
 __device__ __forceinline__ uint32_t mul_hi(uint32_t a, uint32_t b) {
   uint32_t h;
   asm("mul.hi.u32 %0, %1, %2;" : "=r"(h) : "r"(a), "r"(b));
