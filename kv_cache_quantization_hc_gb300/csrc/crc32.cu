@@ -27,12 +27,13 @@
 // register past the group (x^(8 * 512 * kCrcGroup)) and adds each of its words'
 // contributions, read from the map of that word's row position; the register
 // then describes everything the lane has read, with every other lane's bytes
-// taken as zero, positioned at the end of the lane's last word.  A butterfly
-// over the lanes (the lower lane of each pair moves its register 16 * 2^j
-// bytes on and adds its partner's) leaves lane 0 with the segment's register
-// at the segment's end.  Lane 0 moves the first segment's register past the
-// second segment and adds the second's, the initial register's term and the
-// final xor.
+// taken as zero, positioned at the end of the lane's last word, 16 (31 - l)
+// bytes before its segment's end.  Each lane moves its first-segment register
+// past the second segment (a map built from x^(8 * its bytes)) and adds its
+// second-segment register; a butterfly over the lanes (the lower lane of each
+// pair moves its register 16 * 2^j bytes on and adds its partner's) then
+// leaves lane 0 with the unit's register, to which it adds the initial
+// register's term and the final xor.
 //
 // Why rows: giving each lane a contiguous piece of the unit instead (as a first
 // design did) makes a warp's 16-byte loads touch 32 lines 1 KiB apart; that
@@ -54,12 +55,14 @@ struct CrcShared {
   FieldMap<128> word[kCrcGroup];  // word at row position g of a group -> register at the group's end
   FieldMap<32> group;             // a register -> the register kCrcGroup rows later
   FieldMap<32> level[5];          // a register -> the register 16 * 2^j bytes later
+  FieldMap<32> seg2;              // a register -> the register after the second segment
 };
 
 __device__ void build_maps(const CrcParams& p, CrcShared& s) {
   for (int g = 0; g < kCrcGroup; ++g) fill_field_map<128>(s.word[g], p.img_word[g]);
   fill_field_map<32>(s.group, p.img_group);
   for (int j = 0; j < 5; ++j) fill_field_map<32>(s.level[j], p.img_level[j]);
+  fill_field_map<32>(s.seg2, p.img_seg2);
   __syncthreads();
 }
 
@@ -124,18 +127,19 @@ __device__ __forceinline__ int64_t padded_groups(int64_t n_words) {
   return (n_words + 32 * kCrcGroup - 1) / (32 * kCrcGroup);
 }
 
-// A segment of n_words 16-byte words: lane 0 ends with its register at the
-// segment's end.
-__device__ __forceinline__ uint32_t aligned_segment(const CrcShared& s, const uint4* a,
-                                                    int64_t n_words, int lane) {
+// A segment of n_words 16-byte words: the lane's register, at the end of its
+// word in the segment's last row, 16 (31 - lane) bytes before the segment's end.
+__device__ __forceinline__ uint32_t segment_words(const CrcShared& s, const uint4* a,
+                                                  int64_t n_words, int lane) {
   const int64_t groups = padded_groups(n_words);
   const int64_t first = n_words - groups * 32 * kCrcGroup + lane;  // > lane - 128
-  return lane_tree(s, group_range(s, a, first, lane, 0, groups), lane);
+  return group_range(s, a, first, lane, 0, groups);
 }
 
-// Segment 2: t bytes at `at`, then nb bytes at `b`, read byte by byte.
-__device__ __forceinline__ uint32_t byte_segment(const CrcShared& s, const uint8_t* at, int64_t t,
-                                                 const uint8_t* b, int64_t nb, int lane) {
+// Segment 2: t bytes at `at`, then nb bytes at `b`, read byte by byte; the
+// lane's register as for segment_words.
+__device__ __forceinline__ uint32_t segment_bytes(const CrcShared& s, const uint8_t* at, int64_t t,
+                                                  const uint8_t* b, int64_t nb, int lane) {
   const int64_t len = t + nb;
   const int64_t n_words = (len + 15) / 16;
   const int64_t front = 16 * n_words - len;  // zero bytes in front
@@ -160,7 +164,15 @@ __device__ __forceinline__ uint32_t byte_segment(const CrcShared& s, const uint8
     }
     r = c;
   }
-  return lane_tree(s, r, lane);
+  return r;
+}
+
+// Segment 2 alone: lane 0 ends with its register at the segment's end.
+__device__ __forceinline__ uint32_t second_segment(const CrcParams& p, const CrcShared& s,
+                                                   const uint8_t* at, int64_t t, const uint8_t* b,
+                                                   int lane) {
+  return p.b_words ? segment_words(s, reinterpret_cast<const uint4*>(b), p.b_bytes >> 4, lane)
+                   : segment_bytes(s, at, t, b, p.b_bytes, lane);
 }
 
 __global__ void __launch_bounds__(kThreads) k_crc32(const __grid_constant__ CrcParams p) {
@@ -170,14 +182,18 @@ __global__ void __launch_bounds__(kThreads) k_crc32(const __grid_constant__ CrcP
   const int64_t words = p.a_bytes >> 4, t = p.a_bytes & 15;
   for (uint32_t u = blockIdx.x * kWarps + warp; u < p.n_units; u += gridDim.x * kWarps) {
     const uint8_t* a = p.a + static_cast<int64_t>(u) * p.a_stride;
-    uint32_t r1 = words ? aligned_segment(maps, reinterpret_cast<const uint4*>(a), words, lane) : 0u;
-    uint32_t r2 = 0;
+    // Each lane's registers sit 16 (31 - lane) bytes before the end of their
+    // segment; moving the first segment's past the second (seg2) puts both
+    // at the same distance from the unit's end, so one butterfly joins them.
+    uint32_t r = words ? segment_words(maps, reinterpret_cast<const uint4*>(a), words, lane) : 0u;
     if (t + p.b_bytes > 0) {
       const uint8_t* b = p.b_bytes > 0 ? p.b + static_cast<int64_t>(u) * p.b_stride : nullptr;
-      r2 = p.b_words ? aligned_segment(maps, reinterpret_cast<const uint4*>(b), p.b_bytes >> 4, lane)
-                     : byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane);
+      r = apply_map(maps.seg2, r) ^
+          (p.b_words ? segment_words(maps, reinterpret_cast<const uint4*>(b), p.b_bytes >> 4, lane)
+                     : segment_bytes(maps, a + 16 * words, t, b, p.b_bytes, lane));
     }
-    if (lane == 0) p.crc[u] = gf2_mul(r1, p.seg2_shift) ^ r2 ^ p.init_term;
+    r = lane_tree(maps, r, lane);
+    if (lane == 0) p.crc[u] = r ^ p.init_term;
   }
 }
 
@@ -215,10 +231,8 @@ __global__ void __launch_bounds__(kThreads) k_crc32_split(const __grid_constant_
       }
     } else {
       const uint8_t* b = p.b_bytes > 0 ? p.b + u * p.b_stride : nullptr;
-      r = 0;
-      if (t + p.b_bytes > 0)
-        r = p.b_words ? aligned_segment(maps, reinterpret_cast<const uint4*>(b), p.b_bytes >> 4, lane)
-                      : byte_segment(maps, a + 16 * words, t, b, p.b_bytes, lane);
+      r = t + p.b_bytes > 0 ? lane_tree(maps, second_segment(p, maps, a + 16 * words, t, b, lane), lane)
+                            : 0u;
       r ^= p.init_term;
     }
     if (lane == 0) atomicXor(p.crc + u, r);
@@ -263,15 +277,24 @@ cudaError_t launch_crc32(const CrcParams& in, cudaStream_t s) {
   std::memcpy(p.img_level, img.level, sizeof img.level);
   const uint64_t n = static_cast<uint64_t>(p.a_bytes + p.b_bytes);
   p.seg2_shift = crc_x_pow_bytes(static_cast<uint64_t>((p.a_bytes & 15) + p.b_bytes));
+  for (int j = 0; j < 32; ++j) p.img_seg2[j] = gf2_mul(1u << j, p.seg2_shift);
   p.b_words = (p.a_bytes & 15) == 0 && p.b_bytes > 0 && p.b_bytes % 16 == 0 &&
               reinterpret_cast<uintptr_t>(p.b) % 16 == 0 && (p.n_units == 1 || p.b_stride % 16 == 0);
   p.init_term = gf2_mul(0xFFFFFFFFu, crc_x_pow_bytes(n)) ^ 0xFFFFFFFFu;
+  // One warp per unit: a persistent grid of twice the CTAs that fit
+  // nominally (kCrcCtasPerSm per SM; at 40 registers 6 fit), which measured
+  // 1.7% faster than once (3.91 against 3.85 TB/s) and 7% faster than one
+  // CTA per 8 units; 4 times measured 3.80.
+#ifndef HC_CRC_GRID_WAVES
+#define HC_CRC_GRID_WAVES 2
+#endif
   const int64_t resident = static_cast<int64_t>(device_sm_count()) * kCrcCtasPerSm;
   const int64_t groups = (p.a_bytes / 16 + 32 * kCrcGroup - 1) / (32 * kCrcGroup);
   if (static_cast<int64_t>(p.n_units) * 2 >= resident * kWarps || groups < 2 * kCrcMinChunkGroups) {
     // one warp per unit
     const int64_t ctas = (static_cast<int64_t>(p.n_units) + kWarps - 1) / kWarps;
-    k_crc32<<<static_cast<uint32_t>(std::min<int64_t>(ctas, resident)), kThreads, 0, s>>>(p);
+    k_crc32<<<static_cast<uint32_t>(std::min<int64_t>(ctas, resident * HC_CRC_GRID_WAVES)), kThreads, 0,
+              s>>>(p);
     return cudaGetLastError();
   }
   // few, large units: chunks of at least kCrcMinChunkGroups groups, about

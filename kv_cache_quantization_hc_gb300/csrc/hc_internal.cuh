@@ -101,13 +101,14 @@ struct TableParams {
 // CRC-32 of units a[u*a_stride ..+a_bytes) ++ b[u*b_stride ..+b_bytes), one
 // warp per unit (crc32.cu): the unit's rows of 32 16-byte words, lane l
 // taking word l of each row, kCrcGroup rows at a time, by persistent CTAs,
-// kCrcCtasPerSm per SM; a butterfly over the lanes joins their registers,
-// seg2_shift moves the 16-byte-word segment's register past the second
-// segment, and init_term adds the initial register's contribution and the
-// final xor.  Constants are built on the host.  Measured on GB300 over
+// kCrcCtasPerSm per SM; each lane moves its register of the 16-byte-word
+// segment past the second segment (seg2_shift, img_seg2) and adds its
+// register of the second, a butterfly over the lanes joins them, and
+// init_term adds the initial register's contribution and the final xor.  Constants are built on the host.  Measured on GB300 over
 // the Qwen3-8B-shaped FP8 wire (73,728 units of 32 KiB): groups of 4 rows at
 // 8 CTAs/SM 3.43 TB/s (3.68 with the multiply-high field extraction and the
-// scales read as words); at 4 CTAs/SM 3.17; groups of 8 rows 2.2-2.4.
+// scales read as words, 3.92 with one lane butterfly per unit and a grid of
+// twice the nominal CTAs); at 4 CTAs/SM 3.17; groups of 8 rows 2.2-2.4.
 #ifndef HC_CRC_GROUP
 #define HC_CRC_GROUP 4
 #endif
@@ -150,6 +151,7 @@ struct CrcParams {
   uint32_t img_word[kCrcGroup][128];
   uint32_t img_group[32];
   uint32_t img_level[5][32];
+  uint32_t img_seg2[32];  // a register bit j times x^(8 * bytes of the second segment)
 };
 
 // Drift-ranked token selection over n_seq sequences of n_tokens rows of
