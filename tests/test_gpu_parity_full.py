@@ -13,8 +13,11 @@ chunks of blocks), plus properties that hold at any size.
   INT4 (g32, fp16 scales): every block (both block sizes, every padding row)
   of every third layer and the last (13 of 36 layers) is compared with the
   oracle, and placement is checked on all 36; FP8: the first, a middle and
-  the last layer.
+  the last layer.  With HC_PARITY_ALL_LAYERS=1, every block of all 36 layers
+  is compared for both wires (about four more minutes).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -148,7 +151,9 @@ def test_ragged_sweep(wire, pool):
     dev = torch.device("cuda", 0)
     from kv_cache_quantization_hc_gb300 import path as kvpath
     w = workloads.ragged()
-    if wire == "int4":
+    if os.environ.get("HC_PARITY_ALL_LAYERS") == "1":    # every block of every layer
+        all_layers = check_layers = range(w.L)
+    elif wire == "int4":
         all_layers = range(w.L)
         check_layers = set(range(0, w.L, 3)) | {w.L - 1}
     else:
